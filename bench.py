@@ -1,0 +1,589 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed-expert FFN layer on GB300.
+
+One step = one pass of the whole layer (router top-k + softmax, permutation,
+gate/up + SwiGLU, down, ordered combine, shared expert) over one decode window
+of the "decode window" workload: 8 rows (4 batch slots x token + draft
+proposal), hidden 2048, 128 experts top-8, intermediate 768, one shared expert
+of intermediate 768, Zipf(1.1)-biased logits, int4 blocks of 32 with fp16
+scales. Inputs are synthetic (seeded, synth.py) and resident in HBM when the
+timed region starts. The headline value is HBM GB/s over the algorithmic bytes
+of the distinct experts each window touches (plus the shared expert).
+
+Timing: W warm-up steps, then exactly K steps replayed from CUDA graphs,
+bracketed by a barrier and a device synchronise; CUDA events on the launching
+stream; max over ranks. L2 hygiene: consecutive steps rotate over 8 copies of
+the weight pool (2.7 GB), so the weights a window touches have been evicted
+(8 x ~65 MB > 129 MB L2) before the pool copy is used again.
+
+--impl reference times the CPU oracle (the reference arm of this build) on the
+same workload, one sampled row of a window per step, scaled to a window.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer µs & HBM GB/s (decode window); prefill tok/s & tensor-pipe util"
+N_POOLS = 8
+N_WINDOWS = 64
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the secondary configurations (prefill, 48-layer decode, expert cache)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="bound on the oracle's CPU time for cpu_baseline")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- dist
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if _cuda_ok() else "gloo"
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        return self._reduce(v, "max")
+
+    def sum(self, v: float) -> float:
+        return self._reduce(v, "sum")
+
+    def _reduce(self, v, op):
+        if not self.pg:
+            return v
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX if op == "max" else self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def _cuda_ok():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.out, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.out):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.out)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def divisor_le(K: int, cap: int) -> int:
+    for r in range(min(K, cap), 0, -1):
+        if K % r == 0:
+            return r
+    return 1
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "routed_expert_ffn_router_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel sources
+    have not changed since it was taken (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        ent = d.get(workload, {}).get(kernel)
+        if ent and ent.get("csrc_sha") == csrc_hash():
+            return ent.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+    return None
+
+
+# ----------------------------------------------------------------------------- workload
+class DecodeWindowWorkload:
+    """N_POOLS copies of one decode-window layer and N_WINDOWS windows."""
+
+    def __init__(self, torch, synth, cfg, dev, seed=0, n_pools=N_POOLS, n_windows=N_WINDOWS):
+        from routed_expert_ffn_router_gb300.layer import MoeLayer
+        self.cfg = cfg
+        base = synth.make_layer(cfg, seed, device=dev)
+        self.base = base
+        self.layers = [MoeLayer(base, T_max=cfg.T)]
+        for _ in range(n_pools - 1):
+            self.layers.append(MoeLayer(synth.clone_pool(base), T_max=cfg.T))
+        self.logits, self.x = synth.draw_windows(base, n_windows, seed=seed + 1, device=dev)
+        self.outs = [self.layers[0].alloc_outputs(cfg.T) for _ in range(n_windows)]
+        self.n_windows = n_windows
+        self.n_pools = n_pools
+        self.distinct = None
+
+    def step(self, i, stream=None):
+        lay = self.layers[i % self.n_pools]
+        w = i % self.n_windows
+        lay.forward(self.logits[w], self.x[w], out=self.outs[w], stream=stream)
+
+    def count_distinct(self, torch):
+        """Distinct touched resident experts per window (from the routing ids)."""
+        d = []
+        for w in range(self.n_windows):
+            ids = self.outs[w]["ids"]
+            d.append(int(torch.unique(ids).numel()))
+        self.distinct = d
+        return d
+
+    def step_bytes(self, i):
+        cfg = self.cfg
+        D = self.distinct[i % self.n_windows]
+        return D * cfg.expert_bytes() + (cfg.expert_bytes(cfg.shared_I) if cfg.shared_I else 0)
+
+    def kernel_bytes(self, i):
+        """Algorithmic bytes of the gate/up and the down kernel for step i."""
+        cfg = self.cfg
+        D = self.distinct[i % self.n_windows]
+        gu = (D * 2 * cfg.I + (2 * cfg.shared_I if cfg.shared_I else 0)) * cfg.H * 9 // 16
+        dn = (D * cfg.I + cfg.shared_I) * cfg.H * 9 // 16
+        return {"gateup": gu, "down": dn}
+
+
+def capture(torch, fn, n, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            fn(i)
+    return g
+
+
+def time_graph(torch, graphs, reps, stream):
+    """ms for `reps` graph replays on `stream` (replay() launches on the current stream)."""
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        s.record(stream)
+        for r in range(reps):
+            graphs[r % len(graphs)].replay()
+        e.record(stream)
+    e.synchronize()
+    return s.elapsed_time(e)
+
+
+# ----------------------------------------------------------------------------- ours
+def run_ours(args, dist):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from routed_expert_ffn_router_gb300 import _lib, synth
+
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    K, W = args.steps, max(3, args.warmup)
+    cfg = synth.DECODE_WINDOW
+    wl = DecodeWindowWorkload(torch, synth, cfg, dev, seed=dist.rank)
+    stream = torch.cuda.Stream(device=dev)
+
+    # warm-up, eager (also fills the routing outputs used to count bytes)
+    with torch.cuda.stream(stream):
+        for i in range(max(W, wl.n_windows)):
+            wl.step(i, stream)
+    torch.cuda.synchronize()
+    launches_per_step = _lib.moe_last_launch_count()
+    wl.count_distinct(torch)
+    code, bits = wl.layers[0].status()
+    assert code == _lib.MOE_OK, f"device status {bits}"
+
+    # graphs of R consecutive steps; the i-th step of the whole run is step i
+    R = divisor_le(K, 64)
+    n_graphs = max(1, (wl.n_windows * wl.n_pools) // R) if R < 64 else 1
+    n_graphs = min(n_graphs, 8)
+    graphs = []
+    for gi in range(n_graphs):
+        graphs.append(capture(torch, lambda i, b=gi * R: wl.step(b + i, stream), R, stream))
+    torch.cuda.synchronize()
+    reps = K // R
+    for _ in range(2):  # graph warm-up
+        time_graph(torch, graphs, min(reps, len(graphs)), stream)
+
+    clocks = ClockSampler(dist.local)
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ms = time_graph(torch, graphs, reps, stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    dist.barrier()
+    ms_max = dist.max(ms)
+    step_ids = [((r % len(graphs)) * R + i) for r in range(reps) for i in range(R)]
+    bytes_local = sum(wl.step_bytes(i) for i in step_ids)
+    bytes_all = dist.sum(bytes_local)
+    gbs = bytes_all / (ms_max * 1e-3) / 1e9
+    ms_per_step = ms_max / K
+
+    # per-kernel timing: the same graphs re-captured with event pairs around
+    # every kernel; replayed once each and collected
+    _lib.moe_profile_enable(R * launches_per_step * len(graphs) + 64)
+    pgraphs = []
+    for gi in range(len(graphs)):
+        pgraphs.append(capture(torch, lambda i, b=gi * R: wl.step(b + i, stream), R, stream))
+    torch.cuda.synchronize()
+    for g in pgraphs:  # warm-up replays, not collected
+        with torch.cuda.stream(stream):
+            g.replay()
+    torch.cuda.synchronize()
+    n_prof = 0
+    for rep in range(max(1, min(reps, 16))):
+        with torch.cuda.stream(stream):
+            pgraphs[rep % len(pgraphs)].replay()
+        torch.cuda.synchronize()
+        _lib.moe_profile_collect()
+        n_prof += 1
+    totals = _lib.moe_profile_totals()
+    _lib.moe_profile_enable(0)
+    prof_steps = [((r % len(pgraphs)) * R + i) for r in range(n_prof) for i in range(R)]
+    kb = {"gateup": 0, "down": 0}
+    for i in prof_steps:
+        for kk, v in wl.kernel_bytes(i).items():
+            kb[kk] += v
+    hbm_peak, tf_peak, tf_sus, peak_src = load_peaks()
+    kern = {}
+    for name, (tms, cnt) in totals.items():
+        if cnt:
+            kern[name] = {"avg_us": round(tms / cnt * 1e3, 3), "launches": cnt}
+    tot_ms = sum(v[0] for v in totals.values())
+    for name in kern:
+        kern[name]["share"] = round(totals[name][0] / tot_ms, 4) if tot_ms else None
+    dom = max(("gateup", "down"), key=lambda n: totals.get(n, (0, 0))[0])
+    dom_ms, dom_cnt = totals[dom]
+    achieved = (kb[dom] / dom_cnt) / (dom_ms / dom_cnt * 1e-3) / 1e9
+    traffic = ncu_traffic(dom, "decode_window")
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "peak_source": peak_src, "traffic": traffic,
+                "algorithmic_bytes_per_launch": kb[dom] // dom_cnt}
+
+    # end to end through the C ABI with host buffers: H2D of the window's
+    # logits + activations from pinned memory, the layer, D2H of y/ids/w/n_miss
+    e2e = run_e2e(torch, wl, stream, K, R, dist)
+
+    line = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": dist.world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms_per_step, 6),
+        "us_per_layer": round(ms_per_step * 1e3, 3),
+        "rows_per_s": round(cfg.T * dist.world / (ms_per_step * 1e-3), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, random-init int4 experts)",
+        "config": {"workload": "decode_window: 1 layer, T=8 rows, H=2048, E=128 top-8, I=768, "
+                               "shared I=768, Zipf(1.1) logits, int4/32 + fp16 scale",
+                   "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I,
+                   "shared_I": cfg.shared_I,
+                   "l2": f"inputs larger than L2: {N_POOLS} rotating pool copies "
+                         f"({N_POOLS * wl.base.pool_bytes() / 1e9:.2f} GB)",
+                   "parallelism": f"replicas x{dist.world}",
+                   "mean_distinct_experts": round(statistics.mean(wl.distinct), 2)},
+        "roofline": roofline,
+        "kernels": kern,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    if dist.rank == 0 and dist.world == 1 and args.cpu_seconds > 0:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if not args.no_extra and dist.world == 1:
+        try:
+            line["configs"] = extra_configs(torch, synth, _lib, dev, stream, hbm_peak, tf_peak)
+        except Exception as ex:  # the headline line must still print
+            line["configs"] = {"error": f"{type(ex).__name__}: {ex}"}
+    return line
+
+
+def run_e2e(torch, wl, stream, K, R, dist):
+    cfg = wl.cfg
+    lay = wl.layers[0]
+    nw = min(wl.n_windows, 16)
+    h_logits = [wl.logits[w].cpu().pin_memory() for w in range(nw)]
+    h_x = [wl.x[w].cpu().pin_memory() for w in range(nw)]
+    d_logits = torch.empty_like(wl.logits[0])
+    d_x = torch.empty_like(wl.x[0])
+    out = lay.alloc_outputs(cfg.T)
+    h_y = torch.empty(cfg.T, cfg.H, dtype=torch.float32).pin_memory()
+    h_ids = torch.empty(cfg.T, cfg.k, dtype=torch.int32).pin_memory()
+    h_w = torch.empty(cfg.T, cfg.k, dtype=torch.float32).pin_memory()
+    h_nm = torch.empty(1, dtype=torch.int32).pin_memory()
+
+    def step(i):
+        w = i % nw
+        d_logits.copy_(h_logits[w], non_blocking=True)
+        d_x.copy_(h_x[w], non_blocking=True)
+        wl.layers[i % wl.n_pools].forward(d_logits, d_x, out=out, stream=stream)
+        h_y.copy_(out["y"], non_blocking=True)
+        h_ids.copy_(out["ids"], non_blocking=True)
+        h_w.copy_(out["w"], non_blocking=True)
+        h_nm.copy_(out["n_miss"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(4):
+            step(i)
+    torch.cuda.synchronize()
+    g = capture(torch, step, R, stream)
+    torch.cuda.synchronize()
+    time_graph(torch, [g], 2, stream)
+    dist.barrier()
+    torch.cuda.synchronize()
+    ms = time_graph(torch, [g], K // R, stream)
+    ms = dist.max(ms)
+    byts = dist.sum(sum(wl.step_bytes(i % nw) for r in range(K // R) for i in range(R)))
+    bi = h_logits[0].numel() * 4 + h_x[0].numel() * 2
+    bo = h_y.numel() * 4 + h_ids.numel() * 4 + h_w.numel() * 4 + 4
+    return {"value": round(byts / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "us_per_layer": round(ms / K * 1e3, 3), "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo}
+
+
+def cpu_baseline(wl, seconds):
+    """The CPU oracle as it stands on this host, single-threaded, on sampled rows
+    of the same windows; scaled to GB/s of the whole window."""
+    import numpy as np
+    import oracle
+    cfg = wl.cfg
+    host = wl.base.to("cpu")
+    L = oracle.Layer(host)
+    lg = wl.logits.cpu().numpy()
+    xs = wl.x.cpu().numpy()
+    t0 = time.perf_counter()
+    rows_done, byts = 0, 0.0
+    w = 0
+    while time.perf_counter() - t0 < seconds:
+        ids, ww, _ = oracle.route(lg[w], cfg.k)
+        L.rows(ids, ww, rows=[rows_done % cfg.T], x=np.ascontiguousarray(xs[w]))
+        byts += wl.step_bytes(w) / cfg.T  # a row's share of the window's bytes
+        rows_done += 1
+        w = (w + 1) % wl.n_windows
+    el = time.perf_counter() - t0
+    return {"value": round(byts / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows_done} rows of decode windows (1 row each, {el:.1f} s), "
+                      f"window bytes scaled by rows/T",
+            "us_per_layer": round(el / rows_done * cfg.T * 1e6, 1)}
+
+
+# ----------------------------------------------------------------------------- extras
+def extra_configs(torch, synth, _lib, dev, stream, hbm_peak, tf_peak):
+    from routed_expert_ffn_router_gb300.layer import MoeLayer
+    out = {}
+
+    def timed(fn, reps):
+        with torch.cuda.stream(stream):
+            fn(0)
+        torch.cuda.synchronize()
+        g = capture(torch, fn, 1, stream)
+        time_graph(torch, [g], 2, stream)
+        return time_graph(torch, [g], reps, stream) / reps
+
+    # expert cache: 16 rows, H 4096, 256 experts top-8, I 1536, 154 resident
+    cfg = synth.EXPERT_CACHE
+    inp = synth.make_layer(cfg, 0, device=dev)
+    lays = [MoeLayer(inp, cfg.T)] + [MoeLayer(synth.clone_pool(inp), cfg.T) for _ in range(3)]
+    o = lays[0].forward(inp.logits, inp.x)
+    torch.cuda.synchronize()
+    ids = o["ids"]
+    sm = inp.slot_map
+    D = int(torch.unique(ids[(sm[ids.long()] >= 0)]).numel())
+    ms = timed(lambda i: lays[i % 4].forward(inp.logits, inp.x, out=o, stream=stream), 64)
+    byts = D * cfg.expert_bytes()
+    out["expert_cache"] = {"us_per_layer": round(ms * 1e3, 2), "GB/s": round(byts / ms / 1e6, 1),
+                           "frac_hbm": round(byts / ms / 1e6 / hbm_peak, 3),
+                           "distinct_resident": D, "n_miss": int(o["n_miss"].item())}
+    del lays, inp, o
+    torch.cuda.empty_cache()
+
+    # 48 stacked layers, windows of 1..16 rows
+    cfg = synth.DECODE_48
+    layers = [synth.make_layer(cfg, 0, device=dev, layer=l, T=16) for l in range(cfg.layers)]
+    res = {}
+    for T in synth.DECODE48_WINDOWS:
+        mls = [MoeLayer(l, 16) for l in layers]
+        outs = [m.alloc_outputs(T) for m in mls]
+        for m, l, oo in zip(mls, layers, outs):
+            m.forward(l.logits[:T], l.x[:T], out=oo)
+        torch.cuda.synchronize()
+        D = sum(int(torch.unique(oo["ids"]).numel()) for oo in outs)
+
+        def all48(i):
+            for m, l, oo in zip(mls, layers, outs):
+                m.forward(l.logits[:T], l.x[:T], out=oo, stream=stream)
+        ms = timed(all48, 8)
+        byts = D * cfg.expert_bytes()
+        res[f"T{T}"] = {"us_per_layer": round(ms * 1e3 / cfg.layers, 2),
+                        "GB/s": round(byts / ms / 1e6, 1),
+                        "frac_hbm": round(byts / ms / 1e6 / hbm_peak, 3),
+                        "rows_per_s": round(T / (ms * 1e-3 / cfg.layers), 1)}
+    out["decode48"] = res
+    del layers, mls, outs
+    torch.cuda.empty_cache()
+
+    # prefill chunk of 2,048 tokens
+    cfg = synth.PREFILL
+    inp = synth.make_layer(cfg, 0, device=dev)
+    m = MoeLayer(inp, cfg.T)
+    o = m.forward(inp.logits, inp.x)
+    torch.cuda.synchronize()
+    D = int(torch.unique(o["ids"]).numel())
+    ms = timed(lambda i: m.forward(inp.logits, inp.x, out=o, stream=stream), 8)
+    flops = 2 * 3 * cfg.H * cfg.I * (cfg.T * cfg.k) + 2 * 3 * cfg.H * cfg.shared_I * cfg.T
+    out["prefill"] = {"us_per_layer": round(ms * 1e3, 1), "tok_per_s": round(cfg.T / (ms * 1e-3), 1),
+                      "TFLOP/s": round(flops / ms / 1e9, 1),
+                      "frac_bf16_peak": round(flops / ms / 1e9 / tf_peak, 4),
+                      "distinct_experts": D}
+    return out
+
+
+# ----------------------------------------------------------------------------- reference
+def run_reference(args, dist):
+    """The CPU oracle as the reference arm: one sampled row of a decode window
+    per step, scaled to the window; rank 0 only."""
+    import numpy as np
+    import torch
+    import oracle
+    from routed_expert_ffn_router_gb300 import synth
+    if dist.rank != 0:
+        return None
+    cfg = synth.DECODE_WINDOW
+    inp = synth.make_layer(cfg, 0)
+    L = oracle.Layer(inp)
+    logits, xs = synth.draw_windows(inp, 16, seed=1, device="cpu")
+    lg = logits.numpy()
+    xs = xs.numpy()
+    win = []
+    for w in range(16):
+        ids, ww, _ = oracle.route(lg[w], cfg.k)
+        D = len(np.unique(ids))
+        win.append((ids, ww, D * cfg.expert_bytes() + cfg.expert_bytes(cfg.shared_I)))
+
+    def step(i):
+        ids, ww, _ = win[i % 16]
+        L.rows(ids, ww, rows=[i % cfg.T], x=np.ascontiguousarray(xs[i % 16]))
+
+    K, W = args.steps, max(3, args.warmup)
+    for i in range(W):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(K):
+        step(i)
+    el = time.perf_counter() - t0
+    byts = sum(win[i % 16][2] / cfg.T for i in range(K))
+    v = byts / el / 1e9
+    ms_step = el / K * 1e3 * cfg.T  # per window
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "GB/s",
+            "n_gpus": dist.world, "steps": K, "warmup": W, "ms_per_step": round(ms_step, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, random-init int4 experts)",
+            "config": {"workload": "decode_window: 1 layer, T=8 rows, H=2048, E=128 top-8, I=768, "
+                                   "shared I=768, Zipf(1.1) logits, int4/32 + fp16 scale",
+                       "sample": "one row of a window per step, bytes scaled by 1/T"},
+            "cpu_baseline": {"value": round(v, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{K} steps x 1 row"},
+            "e2e": {"value": round(v, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            line = run_reference(args, dist)
+        else:
+            line = run_ours(args, dist)
+        if dist.rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,158 @@
+// Shared device helpers of the sm_103a routed-expert FFN library.
+//
+// Inline PTX wrappers (mbarrier, bulk async copy, warp MMA, LOP3), the
+// workspace layout and the device-status bits. Written for sm_103a only.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- status bits
+// Device-detected problems are OR-ed into the workspace status word; kernels
+// never trap. moe_read_status() maps them back to moe_status codes.
+enum : int32_t {
+  DEV_NONFINITE_LOGIT = 1,   // a router logit was NaN or infinite
+  DEV_BAD_SLOT = 2,          // slot_map[e] >= S (treated as not resident)
+  DEV_TIMEOUT = 4,           // a bounded wait expired
+  DEV_RANGE = 8,             // an activation outside the fp16 range (prefill path)
+};
+
+constexpr int kMaxK = 32;
+constexpr int kMaxE = 1024;
+constexpr int kTokTile = 16;          // token slots per decode unit (two n8 MMA tiles)
+constexpr int kRowTile = 16;          // weight rows per decode unit (one m16 MMA tile)
+constexpr int kWarps = 8;             // warps per decode CTA (split K)
+constexpr float kMagic = 136.0f;      // bf16 0x4300|n' = 128 + (q ^ 8) = 136 + q
+
+// ---------------------------------------------------------------- workspace
+// All offsets are 256-byte aligned. The layout depends only on (desc, T).
+struct WsLayout {
+  size_t status, counters, offsets, sorted_pair, pair_pos, act, cu, hist;
+  size_t xhi, xlo, xcorr, hhi, hlo, hsum, partial, total;
+  int P, Imax, n_chunks, cu_max;
+};
+
+__host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Per-active-expert record written by the permutation for the FFN kernels.
+struct ActExpert {
+  int32_t e;      // expert id (-1 for the shared expert)
+  int32_t slot;   // pool slot (-1 for the shared expert)
+  int32_t off;    // first row of this expert in the h / partial buffers
+  int32_t cnt;    // rows routed to it
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// Bulk async copy global -> this CTA's shared memory, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of `bar`, giving up after ~1 s: then the status word
+// gets DEV_TIMEOUT and the caller skips its work. Returns true on success.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  int32_t* status) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (it == 0) t0 = globaltimer_ns();
+    else if ((it & 63) == 0 && globaltimer_ns() - t0 > 1000000000ull) {
+      if (status) atomicOr(status, DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// f = (a & b) ^ c
+__device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Four bf16x2 registers from one 32-bit word of int4 codes (nibble i = column
+// 8c+i of the block). Register r holds (column 8c+r, column 8c+r+4) as the
+// bf16 values 136 + code: lop3 drops nibble r and r+4 into the low mantissa bits
+// of the bf16 constant 128 (0x4300) and flips bit 3, which maps a two's
+// complement code q to q + 8.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&d)[4]) {
+  const uint32_t mask = 0x000F000Fu, magic = 0x43084308u;
+  d[0] = lop3_and_xor(w, mask, magic);
+  d[1] = lop3_and_xor(w >> 4, mask, magic);
+  d[2] = lop3_and_xor(w >> 8, mask, magic);
+  d[3] = lop3_and_xor(w >> 12, mask, magic);
+}
+
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Position of column j (0..7) of an 8-column group in the fragment order
+// [0,4,1,5,2,6,3,7] used for the MMA B operand.
+__host__ __device__ __forceinline__ int perm8_pos(int j) { return 2 * (j & 3) + (j >> 2); }
+
+__device__ __forceinline__ uint16_t bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ float bf16_to_f(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+}  // namespace moe

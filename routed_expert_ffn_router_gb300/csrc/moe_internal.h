@@ -1,0 +1,78 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+// Kernel kinds for the optional event timing (moe_profile_*).
+enum KernelKind : int {
+  K_ROUTER_LOGITS = 0, K_ROUTE, K_PERMUTE, K_X_PREP, K_GATEUP, K_DOWN, K_COMBINE, K_NUM_KINDS
+};
+
+// Every kernel launch is bracketed by these: they count launches and, when
+// timing is enabled, record a CUDA event pair on the launching stream.
+void launch_begin(int kind, cudaStream_t st);
+void launch_end(cudaStream_t st);
+
+// Sizes the host validated; everything a launch needs besides pointers.
+struct Shape {
+  int H, I, shI, E, k, S, T, P, Imax;
+};
+
+WsLayout ws_layout(int E, int k, int T, int H, int I, int shI);
+
+struct PermuteOut {
+  int32_t* offsets;
+  int32_t* sorted_pair;
+  int32_t* pair_pos;
+  int32_t* miss_ids;
+  int32_t* n_miss;
+  ActExpert* act;
+  int2* cu;          // column units: (active index, token chunk of 16)
+  int32_t* counters;  // [0] active experts incl. shared, [1] column units
+  int32_t* hist;      // chunked path scratch [n_chunks][E]
+  int32_t* status;
+};
+
+struct FfnArgs {
+  const uint8_t *gq, *uq, *dq;
+  const uint16_t *gs, *us, *ds;
+  const uint8_t *sgq, *suq, *sdq;
+  const uint16_t *sgs, *sus, *sds;
+  int H, I, shI, E, k, S, T, P, Imax;
+  const int32_t* sorted_pair;
+  const int32_t* pair_pos;
+  const int32_t* ids;
+  const float* w;
+  const int32_t* slot_map;
+  const ActExpert* act;
+  const int2* cu;
+  const int32_t* counters;
+  const uint16_t* xhi;
+  const uint16_t* xlo;
+  const float* xcorr;
+  uint16_t* hhi;
+  uint16_t* hlo;
+  float* hsum;
+  float* partial;
+  float* y;
+  int32_t* status;
+};
+
+cudaError_t launch_router_logits(const void* x, bool x_bf16, const float* wg, int T, int H, int E,
+                                 float* logits, cudaStream_t st);
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                         int32_t* status, cudaStream_t st);
+cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, const int32_t* slot_map, int S,
+                           bool has_shared, const PermuteOut& o, cudaStream_t st);
+cudaError_t launch_ffn_decode(const FfnArgs& a, const void* x, bool x_bf16, int cu_max,
+                              cudaStream_t st);
+
+int cu_bound(int T, int E, int k, bool has_shared);
+
+}  // namespace moe

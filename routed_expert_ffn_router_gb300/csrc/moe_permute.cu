@@ -1,0 +1,242 @@
+// (token, expert) permutation: a deterministic counting sort of the P = T*k
+// pairs by expert, stable in the pair index p = t*k + j (the expert-scoped
+// layout of the SGLang port post, section 2), plus the slot-map lookup and the
+// list of missing experts ("extended-strata-moe reference", "The mailbox"
+// step 1; misses counted as distinct experts per layer, "C API").
+//
+// No order-dependent atomics decide a position: counts use integer atomics
+// (order-free), positions come from prefix sums and an explicit rank of each
+// pair among the earlier pairs of its expert.
+#include "moe_internal.h"
+
+namespace moe {
+
+constexpr int kChunk = 1024;  // pairs per CTA in the chunked path
+
+// Exclusive prefix sum over a 1024-thread block; *total receives the sum.
+__device__ int block_excl_scan(int v, int* s_warp, int* s_total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int wv = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, wv, off);
+      if (lane >= off) wv += y;
+    }
+    s_warp[lane] = wv;
+    if (lane == 31) *s_total = wv;
+  }
+  __syncthreads();
+  int base = warp > 0 ? s_warp[warp - 1] : 0;
+  int res = base + x - v;
+  __syncthreads();
+  return res;
+}
+
+// Miss list, active-expert records and token-chunk work units, from the
+// per-expert counts and offsets held in shared memory. Thread e handles
+// expert e (blockDim >= E).
+__device__ void build_lists(int E, int P, int T, int S, bool has_shared,
+                            const int32_t* __restrict__ slot_map, const int* s_cnt,
+                            const int* s_off, int* s_warp, int* s_total, const PermuteOut& o) {
+  const int e = threadIdx.x;
+  int c = e < E ? s_cnt[e] : 0;
+  int slot = -1;
+  if (c > 0) {
+    slot = slot_map ? slot_map[e] : e;
+    if (slot >= S) {
+      atomicOr(o.status, DEV_BAD_SLOT);
+      slot = -1;
+    }
+  }
+  const int is_miss = (c > 0 && slot < 0) ? 1 : 0;
+  const int is_act = (c > 0 && slot >= 0) ? 1 : 0;
+  int mi = block_excl_scan(is_miss, s_warp, s_total);
+  const int n_miss = *s_total;
+  __syncthreads();
+  int ai = block_excl_scan(is_act, s_warp, s_total);
+  const int n_act = *s_total;
+  __syncthreads();
+  const int chunks = is_act ? (c + kTokTile - 1) / kTokTile : 0;
+  int ci = block_excl_scan(chunks, s_warp, s_total);
+  const int n_cu_routed = *s_total;
+  __syncthreads();
+  if (is_miss) o.miss_ids[mi] = e;
+  if (is_act) {
+    ActExpert r;
+    r.e = e;
+    r.slot = slot;
+    r.off = s_off[e];
+    r.cnt = c;
+    o.act[ai] = r;
+    for (int q = 0; q < chunks; ++q) o.cu[ci + q] = make_int2(ai, q);
+  }
+  const int sh_chunks = has_shared ? (T + kTokTile - 1) / kTokTile : 0;
+  for (int q = threadIdx.x; q < sh_chunks; q += blockDim.x) o.cu[n_cu_routed + q] = make_int2(n_act, q);
+  if (threadIdx.x == 0) {
+    *o.n_miss = n_miss;
+    if (has_shared) {
+      ActExpert r;
+      r.e = -1;
+      r.slot = -1;
+      r.off = P;
+      r.cnt = T;
+      o.act[n_act] = r;
+    }
+    o.counters[0] = n_act + (has_shared ? 1 : 0);
+    o.counters[1] = n_cu_routed + sh_chunks;
+  }
+}
+
+__device__ __forceinline__ int load_id(const int32_t* ids, int p, int E, int32_t* status) {
+  int e = ids[p];
+  if (e < 0 || e >= E) {
+    atomicOr(status, DEV_BAD_SLOT);
+    e = e < 0 ? 0 : E - 1;
+  }
+  return e;
+}
+
+// P <= 1024: everything in one CTA.
+__global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ ids, int T,
+                                                             int E, int k,
+                                                             const int32_t* __restrict__ slot_map,
+                                                             int S, int has_shared, PermuteOut o) {
+  __shared__ int s_ids[kChunk];
+  __shared__ int s_cnt[kMaxE];
+  __shared__ int s_off[kMaxE + 1];
+  __shared__ int s_warp[32];
+  __shared__ int s_total;
+  const int tid = threadIdx.x;
+  const int P = T * k;
+  int e = 0;
+  if (tid < P) {
+    e = load_id(ids, tid, E, o.status);
+    s_ids[tid] = e;
+  }
+  if (tid < E) s_cnt[tid] = 0;
+  __syncthreads();
+  if (tid < P) atomicAdd(&s_cnt[e], 1);
+  __syncthreads();
+  int off = block_excl_scan(tid < E ? s_cnt[tid] : 0, s_warp, &s_total);
+  if (tid < E) s_off[tid] = off;
+  if (tid == 0) s_off[E] = P;
+  __syncthreads();
+  if (tid < P) {
+    int rank = 0;
+    for (int q = 0; q < tid; ++q) rank += (s_ids[q] == e) ? 1 : 0;
+    int pos = s_off[e] + rank;
+    o.sorted_pair[pos] = tid;
+    o.pair_pos[tid] = pos;
+  }
+  if (tid < E) o.offsets[tid] = s_off[tid];
+  if (tid == 0) o.offsets[E] = P;
+  build_lists(E, P, T, S, has_shared != 0, slot_map, s_cnt, s_off, s_warp, &s_total, o);
+}
+
+// Chunked path, step 1: per-chunk histograms hist[c][e].
+__global__ void __launch_bounds__(1024) permute_hist_kernel(const int32_t* __restrict__ ids, int P,
+                                                            int E, PermuteOut o) {
+  __shared__ int s_cnt[kMaxE];
+  const int tid = threadIdx.x;
+  if (tid < E) s_cnt[tid] = 0;
+  __syncthreads();
+  int p = blockIdx.x * kChunk + tid;
+  if (p < P) atomicAdd(&s_cnt[load_id(ids, p, E, o.status)], 1);
+  __syncthreads();
+  if (tid < E) o.hist[(size_t)blockIdx.x * E + tid] = s_cnt[tid];
+}
+
+// Step 2 (one CTA): per expert, chunk bases in chunk order (hist becomes the
+// exclusive base), totals, offsets, then the lists.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int k, int n_chunks,
+                                                            const int32_t* __restrict__ slot_map,
+                                                            int S, int has_shared, PermuteOut o) {
+  __shared__ int s_cnt[kMaxE];
+  __shared__ int s_off[kMaxE + 1];
+  __shared__ int s_warp[32];
+  __shared__ int s_total;
+  const int tid = threadIdx.x;
+  const int P = T * k;
+  int run = 0;
+  if (tid < E) {
+    for (int c = 0; c < n_chunks; ++c) {
+      int h = o.hist[(size_t)c * E + tid];
+      o.hist[(size_t)c * E + tid] = run;
+      run += h;
+    }
+    s_cnt[tid] = run;
+  }
+  __syncthreads();
+  int off = block_excl_scan(tid < E ? run : 0, s_warp, &s_total);
+  if (tid < E) s_off[tid] = off;
+  if (tid == 0) s_off[E] = P;
+  __syncthreads();
+  if (tid < E) o.offsets[tid] = s_off[tid];
+  if (tid == 0) o.offsets[E] = P;
+  build_lists(E, P, T, S, has_shared != 0, slot_map, s_cnt, s_off, s_warp, &s_total, o);
+}
+
+// Step 3: position = offsets[e] + base of this chunk for e + rank inside the chunk.
+__global__ void __launch_bounds__(1024) permute_scatter_kernel(const int32_t* __restrict__ ids,
+                                                               int P, int E, PermuteOut o) {
+  __shared__ int s_ids[kChunk];
+  const int tid = threadIdx.x;
+  const int p0 = blockIdx.x * kChunk;
+  const int n = min(kChunk, P - p0);
+  int e = 0;
+  if (tid < n) {
+    e = load_id(ids, p0 + tid, E, o.status);
+    s_ids[tid] = e;
+  }
+  __syncthreads();
+  if (tid < n) {
+    int rank = 0;
+    for (int q = 0; q < tid; ++q) rank += (s_ids[q] == e) ? 1 : 0;
+    int pos = o.offsets[e] + o.hist[(size_t)blockIdx.x * E + e] + rank;
+    o.sorted_pair[pos] = p0 + tid;
+    o.pair_pos[p0 + tid] = pos;
+  }
+}
+
+int cu_bound(int T, int E, int k, bool has_shared) {
+  const int P = T * k;
+  const int sh = has_shared ? (T + kTokTile - 1) / kTokTile : 0;
+  if (T <= kTokTile) return (P < E ? P : E) + sh;
+  // sum_e ceil(c_e/16) <= P/16 + (number of experts touched)
+  return P / kTokTile + (P < E ? P : E) + sh;
+}
+
+cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, const int32_t* slot_map, int S,
+                           bool has_shared, const PermuteOut& o, cudaStream_t st) {
+  const int P = T * k;
+  if (P <= kChunk) {
+    launch_begin(K_PERMUTE, st);
+    permute_small_kernel<<<1, 1024, 0, st>>>(ids, T, E, k, slot_map, S, has_shared ? 1 : 0, o);
+    launch_end(st);
+    return cudaGetLastError();
+  }
+  const int nc = (P + kChunk - 1) / kChunk;
+  launch_begin(K_PERMUTE, st);
+  permute_hist_kernel<<<nc, 1024, 0, st>>>(ids, P, E, o);
+  launch_end(st);
+  launch_begin(K_PERMUTE, st);
+  permute_scan_kernel<<<1, 1024, 0, st>>>(T, E, k, nc, slot_map, S, has_shared ? 1 : 0, o);
+  launch_end(st);
+  launch_begin(K_PERMUTE, st);
+  permute_scatter_kernel<<<nc, 1024, 0, st>>>(ids, P, E, o);
+  launch_end(st);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

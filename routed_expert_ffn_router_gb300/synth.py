@@ -217,6 +217,29 @@ def make_layer(cfg: MoeConfig, seed: int = 0, device="cpu", layer: int = 0,
                        slot_map=slot_map, S=S, sh=sh, **pool)
 
 
+def draw_windows(inp: LayerInputs, n: int, seed: int, device=None):
+    """n more (logits, x) windows for the same layer: same popularity ranks, fresh
+    noise and activations. Returns (logits [n, T, E] f32, x [n, T, H])."""
+    cfg = inp.cfg
+    device = inp.x.device if device is None else device
+    T = inp.x.shape[0]
+    g = _gen(seed * 7_919 + 17, device)
+    bias = -cfg.zipf_s * torch.log(inp.rank.to(device).double()).float()
+    logits = torch.randn(n, T, cfg.E, generator=g, device=device) + bias
+    x = torch.randn(n, T, cfg.H, generator=g, device=device)
+    if cfg.x_dtype == "bf16":
+        x = f32_to_bf16_bits(x)
+    return logits.contiguous(), x.contiguous()
+
+
+def clone_pool(inp: LayerInputs) -> LayerInputs:
+    """A copy of the layer with its own weight-pool buffers (same bytes)."""
+    sh = None if inp.sh is None else {k: v.clone() for k, v in inp.sh.items()}
+    return dataclasses.replace(inp, gate_q=inp.gate_q.clone(), gate_s=inp.gate_s.clone(),
+                               up_q=inp.up_q.clone(), up_s=inp.up_s.clone(),
+                               down_q=inp.down_q.clone(), down_s=inp.down_s.clone(), sh=sh)
+
+
 def random_slot_map(E: int, frac: float, seed: int) -> torch.Tensor:
     """Seeded random residency (used to exercise the miss path): slots in id order."""
     g = _gen(seed, "cpu")

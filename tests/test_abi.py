@@ -1,0 +1,108 @@
+"""The C-ABI library loads, exports every entry point of include/moe.h, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from routed_expert_ffn_router_gb300 import _lib
+from routed_expert_ffn_router_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return _lib.load()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in moe.h but not exported"
+    assert set(names) == set(_lib.EXPORTS)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert _lib.status_str(code)
+    assert _lib.status_str(99) == "unknown status"
+
+
+def _desc(H=256, I=128, E=8, k=2, S=8, shared_I=0, ptr=4096):
+    d = _lib.moe_layer_desc()
+    d.H, d.I, d.E, d.k, d.S, d.shared_I = H, I, E, k, S, shared_I
+    for f in ("gate", "up", "down", "shared_gate", "shared_up", "shared_down"):
+        setattr(d, f, _lib.moe_qmat(ptr, ptr))
+    return d
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(E=0), _lib.MOE_ERR_INVALID),
+    (dict(E=1025, k=2), _lib.MOE_ERR_UNSUPPORTED),
+    (dict(k=33, E=64), _lib.MOE_ERR_UNSUPPORTED),
+    (dict(k=9, E=8), _lib.MOE_ERR_UNSUPPORTED),
+    (dict(H=200), _lib.MOE_ERR_UNSUPPORTED),
+    (dict(I=64), _lib.MOE_ERR_INVALID),
+    (dict(S=0), _lib.MOE_ERR_INVALID),
+    (dict(ptr=4097), _lib.MOE_ERR_INVALID),
+    (dict(ptr=0), _lib.MOE_ERR_INVALID),
+    (dict(shared_I=96), _lib.MOE_ERR_UNSUPPORTED),
+])
+def test_desc_validation(lib, kw, code):
+    d = _desc(**kw)
+    assert lib.moe_workspace_bytes(ctypes.byref(d), 4) == 0
+    rc = lib.moe_expert_ffn(ctypes.byref(d), 4096, 1, 4, 4096, 4096, None, 4096, 4096, 4096, 4096,
+                            1 << 30, None)
+    assert rc == code
+
+
+def test_workspace_checks(lib):
+    d = _desc()
+    need = lib.moe_workspace_bytes(ctypes.byref(d), 4)
+    assert need > 0
+    assert lib.moe_workspace_bytes(ctypes.byref(d), 64) > need
+    # too small, misaligned, null
+    assert lib.moe_expert_ffn(ctypes.byref(d), 4096, 1, 4, 4096, 4096, None, 4096, 4096, 4096, 4096,
+                              need - 1, None) == _lib.MOE_ERR_WORKSPACE
+    assert lib.moe_expert_ffn(ctypes.byref(d), 4096, 1, 4, 4096, 4096, None, 4096, 4096, 4096,
+                              4096 + 16, need, None) == _lib.MOE_ERR_WORKSPACE
+    assert lib.moe_expert_ffn(ctypes.byref(d), 4096, 1, 4, 4096, 4096, None, 4096, 4096, 4096, None,
+                              need, None) == _lib.MOE_ERR_WORKSPACE
+    # a bad dtype, a negative T, missing miss-list buffers
+    assert lib.moe_expert_ffn(ctypes.byref(d), 4096, 7, 4, 4096, 4096, None, 4096, 4096, 4096, 4096,
+                              need, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_expert_ffn(ctypes.byref(d), 4096, 1, -1, 4096, 4096, None, 4096, 4096, 4096, 4096,
+                              need, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_expert_ffn(ctypes.byref(d), 4096, 1, 4, 4096, 4096, None, 4096, None, 4096, 4096,
+                              need, None) == _lib.MOE_ERR_INVALID
+
+
+def test_route_and_permute_validation(lib):
+    assert lib.moe_route(4096, 4, 0, 1, 4096, 4096, None, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_route(4096, 4, 8, 9, 4096, 4096, None, None) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(4096, -1, 8, 2, 4096, 4096, None, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_route(None, 4, 8, 2, 4096, 4096, None, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_route(None, 0, 8, 2, None, None, None, None) == _lib.MOE_OK  # T = 0: no-op
+    assert lib.moe_permute(4096, 4, 8, 2, None, 0, 4096, 4096, 4096, 4096, 4096, 4096, 1 << 20,
+                           None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_permute(4096, 4, 8, 2, None, 8, 4096, 4096, 4096, 4096, 4096, None, 1 << 20,
+                           None) == _lib.MOE_ERR_WORKSPACE
+
+
+def test_workspace_grows_with_T(lib):
+    d = _desc(H=2048, I=768, E=128, k=8, S=128, shared_I=768)
+    prev = 0
+    for T in (0, 1, 8, 16, 64, 2048):
+        n = lib.moe_workspace_bytes(ctypes.byref(d), T)
+        assert n >= prev and n % 256 == 0
+        prev = n

@@ -1,0 +1,327 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Routing (ids, fp32 weights), the permutation and the miss list must match bit
+for bit; layer outputs within max|y - y_oracle| <= 2e-3 * max|y_oracle| over the
+rows checked. Full-size configurations are checked on every row the oracle can
+afford and on sampled rows for the 2,048-token chunk.
+"""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from routed_expert_ffn_router_gb300 import _lib, synth
+from routed_expert_ffn_router_gb300 import build as libbuild
+from routed_expert_ffn_router_gb300.layer import MoeLayer
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    libbuild.build()
+    _lib.load()
+
+
+def assert_weights_match(w_gpu, w_orc, w_exact):
+    """Bitwise, except that a weight whose exact value sits at an fp32 rounding
+    midpoint (within 2^-40 relative) may round to either neighbour."""
+    w_gpu = np.asarray(w_gpu, np.float32)
+    bad = np.argwhere(w_gpu != w_orc)
+    for idx in bad:
+        idx = tuple(idx)
+        a, b = w_gpu[idx], w_orc[idx]
+        assert abs(int(a.view(np.int32)) - int(b.view(np.int32))) == 1, (idx, a, b)
+        mid = (float(a) + float(b)) / 2
+        assert abs(w_exact[idx] - mid) <= 2.0 ** -40 * abs(mid), (idx, a, b, w_exact[idx])
+
+
+def check_y(y_gpu, y_ref, tol=TOL, what=""):
+    y_gpu = np.asarray(y_gpu, np.float64)
+    err = np.abs(y_gpu - y_ref).max()
+    scale = np.abs(y_ref).max()
+    assert np.all(np.isfinite(y_gpu)), what
+    assert err <= tol * scale, f"{what}: max|dy| = {err:.3e}, max|y| = {scale:.3e}, ratio {err / scale:.3e}"
+    return err / scale
+
+
+def gpu_route(logits_np, k):
+    T, E = logits_np.shape
+    lg = torch.from_numpy(np.ascontiguousarray(logits_np)).to(DEV)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    _lib.moe_route(lg, T, E, k, ids, w, st)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy(), int(st.item())
+
+
+# ---------------------------------------------------------------- router
+@pytest.mark.parametrize("xbf16", [False, True])
+def test_router_logits_bit_exact(xbf16):
+    cfg = synth.TINY if not xbf16 else synth.MoeConfig("tb", H=256, I=128, E=8, k=2, T=4,
+                                                       router_from_x=True)
+    inp = synth.make_layer(cfg, 0)
+    lg_ref = oracle.router_logits(synth.bf16_bits_to_f32(inp.x.numpy()) if xbf16 else inp.x, inp.wg)
+    x = inp.x.to(DEV)
+    wg = inp.wg.to(DEV)
+    out = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=DEV)
+    _lib.moe_router_logits(x, _lib.MOE_BF16 if xbf16 else _lib.MOE_F32, wg, cfg.T, cfg.H, cfg.E, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().view(np.int32), lg_ref.view(np.int32))
+
+
+ROUTE_CASES = [("tiny", 4, 8, 2, 0.0), ("decode_window", 8, 128, 8, 1.1),
+               ("decode48_T1", 1, 512, 10, 1.0), ("decode48_T16", 16, 512, 10, 1.0),
+               ("expert_cache", 16, 256, 8, 1.2), ("prefill", 2048, 512, 10, 1.0),
+               ("maxE_maxk", 64, 1024, 32, 0.5), ("k_eq_E", 9, 7, 7, 0.0), ("E1", 5, 1, 1, 0.0)]
+
+
+@pytest.mark.parametrize("name,T,E,k,s", ROUTE_CASES)
+def test_route_bit_exact(name, T, E, k, s):
+    lg = synth.random_logits(T, E, seed=T * 7 + E, zipf_s=s).numpy()
+    ids_o, w_o, we = oracle.route(lg, k)
+    ids, w, st = gpu_route(lg, k)
+    assert st == 0
+    assert np.array_equal(ids, ids_o)
+    assert_weights_match(w, w_o, we)
+
+
+def test_route_ties_go_to_lower_id():
+    rng = np.random.default_rng(3)
+    lg = (np.round(rng.normal(size=(300, 64)) * 2) / 2).astype(np.float32)  # many exact ties
+    lg[0] = 0.0
+    lg[1, :] = -0.0
+    lg[1, 10] = 0.0
+    ids_o, w_o, we = oracle.route(lg, 10)
+    ids, w, st = gpu_route(lg, 10)
+    assert np.array_equal(ids, ids_o)
+    assert list(ids[0]) == list(range(10))
+    assert_weights_match(w, w_o, we)
+
+
+def test_route_flags_non_finite():
+    lg = synth.random_logits(4, 32, seed=1).numpy()
+    lg[2, 5] = np.inf
+    _, _, st = gpu_route(lg, 4)
+    assert st & 1
+
+
+# ---------------------------------------------------------------- permutation
+def gpu_permute(ids_np, E, slot_map=None, S=None):
+    T, k = ids_np.shape
+    P = T * k
+    ids = torch.from_numpy(np.ascontiguousarray(ids_np)).to(DEV)
+    off = torch.full((E + 1,), -7, dtype=torch.int32, device=DEV)
+    sp = torch.full((max(P, 1),), -7, dtype=torch.int32, device=DEV)
+    pp = torch.full((max(P, 1),), -7, dtype=torch.int32, device=DEV)
+    miss = torch.full((E,), -7, dtype=torch.int32, device=DEV)
+    nm = torch.full((1,), -7, dtype=torch.int32, device=DEV)
+    ws_bytes = 1 << 22
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=DEV)
+    sm = None if slot_map is None else torch.from_numpy(np.asarray(slot_map, np.int32)).to(DEV)
+    _lib.moe_permute(ids, T, E, k, sm, E if S is None else S, off, sp, pp, miss, nm, ws, ws_bytes)
+    torch.cuda.synchronize()
+    n = int(nm.item())
+    return dict(offsets=off.cpu().numpy(), sorted_pair=sp.cpu().numpy()[:P],
+                pair_pos=pp.cpu().numpy()[:P], miss_ids=miss.cpu().numpy()[:n], n_miss=n,
+                status=int(ws[:4].view(torch.int32).item()))
+
+
+@pytest.mark.parametrize("name,T,E,k,s", ROUTE_CASES + [("chunked", 300, 64, 8, 1.0),
+                                                        ("ragged", 103, 96, 10, 1.0)])
+@pytest.mark.parametrize("resident", [1.0, 0.6, 0.0])
+def test_permute_bit_exact(name, T, E, k, s, resident):
+    lg = synth.random_logits(T, E, seed=T + 3 * E, zipf_s=s).numpy()
+    ids, _, _ = oracle.route(lg, k)
+    if resident == 1.0:
+        sm, S = None, E
+    else:
+        smt, S = synth.random_slot_map(E, resident, seed=E)
+        sm = smt.numpy()
+        S = max(S, 1)
+    ref = oracle.permute(ids, E, sm)
+    got = gpu_permute(ids, E, sm, S)
+    assert got["status"] == 0
+    for key in ("offsets", "sorted_pair", "pair_pos", "miss_ids"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert got["n_miss"] == ref["n_miss"]
+
+
+def test_permute_flags_slot_out_of_range():
+    ids = np.array([[0, 1], [2, 1]], np.int32)
+    got = gpu_permute(ids, 4, np.array([0, 5, 1, -1], np.int32), S=3)
+    assert got["status"] & 2
+    assert list(got["miss_ids"]) == [1]  # treated as not resident
+
+
+# ---------------------------------------------------------------- layer
+def run_layer(inp, logits=None, x=None, slot_map="default", lay=None):
+    dev_inp = inp if inp.gate_q.is_cuda else inp.to(DEV)
+    lay = lay or MoeLayer(dev_inp, T_max=(x if x is not None else inp.x).shape[0])
+    lg = (inp.logits if logits is None else logits).to(DEV)
+    xx = (inp.x if x is None else x).to(DEV)
+    sm = slot_map if isinstance(slot_map, str) else (None if slot_map is None else slot_map.to(DEV))
+    out = lay.forward(lg, xx, slot_map=sm)
+    torch.cuda.synchronize()
+    code, bits = lay.status()
+    assert code == _lib.MOE_OK, bits
+    return {k: v.cpu().numpy() for k, v in out.items()}, lay
+
+
+def oracle_layer(inp, logits, rows=None, slot_map="default"):
+    ids, w, we = oracle.route(np.asarray(logits), inp.cfg.k)
+    L = oracle.Layer(inp)
+    y = L.rows(ids, w, rows=rows, slot_map=slot_map)
+    return ids, w, we, y
+
+
+def test_tiny_layer_end_to_end():
+    """Tiny case: router GEMV on the GPU, then route + FFN, against the oracle."""
+    cfg = synth.TINY
+    inp = synth.make_layer(cfg, 0)
+    lg = oracle.router_logits(inp.x, inp.wg)
+    dinp = inp.to(DEV)
+    lg_dev = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=DEV)
+    _lib.moe_router_logits(dinp.x, _lib.MOE_F32, dinp.wg, cfg.T, cfg.H, cfg.E, lg_dev)
+    out, _ = run_layer(dinp, logits=lg_dev)
+    ids, w, we, y = oracle_layer(inp, lg)
+    assert np.array_equal(out["ids"], ids)
+    assert_weights_match(out["w"], w, we)
+    check_y(out["y"], y, what="tiny")
+    assert out["n_miss"][0] == 0
+
+
+@pytest.mark.parametrize("cfg", [synth.DECODE_WINDOW, synth.EXPERT_CACHE], ids=lambda c: c.name)
+def test_decode_configs_full(cfg):
+    inp = synth.make_layer(cfg, 0, device=DEV)
+    out, _ = run_layer(inp)
+    hinp = inp.to("cpu")
+    ids, w, we, y = oracle_layer(hinp, hinp.logits.numpy())
+    assert np.array_equal(out["ids"], ids)
+    assert_weights_match(out["w"], w, we)
+    pm = oracle.permute(ids, cfg.E, None if hinp.slot_map is None else hinp.slot_map.numpy())
+    assert out["n_miss"][0] == pm["n_miss"]
+    assert np.array_equal(out["miss_ids"][:pm["n_miss"]], pm["miss_ids"])
+    check_y(out["y"], y, what=cfg.name)
+
+
+@pytest.mark.parametrize("T", synth.DECODE48_WINDOWS)
+def test_decode48_layers(T):
+    """Large-expert-count decode: two of the 48 layers (first and last seed
+    streams) at every window size."""
+    cfg = synth.DECODE_48
+    for layer in (0, 47):
+        inp = synth.make_layer(cfg, 0, device=DEV, layer=layer, T=T)
+        out, _ = run_layer(inp)
+        hinp = inp.to("cpu")
+        ids, w, we, y = oracle_layer(hinp, hinp.logits.numpy())
+        assert np.array_equal(out["ids"], ids)
+        check_y(out["y"], y, what=f"decode48 T={T} layer {layer}")
+
+
+def test_expert_cache_random_slot_map_and_misses():
+    cfg = synth.MoeConfig("ec_small", H=1024, I=512, E=64, k=8, T=16, zipf_s=1.2)
+    inp = synth.make_layer(cfg, 5)
+    smt, S = synth.random_slot_map(cfg.E, 0.6, seed=9)
+    # pool with only the resident experts: slot s = the s-th resident expert
+    keep = (smt >= 0).nonzero().flatten()
+    for kname in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s"):
+        setattr(inp, kname, getattr(inp, kname)[keep].contiguous())
+    inp.S = S
+    inp.slot_map = smt
+    out, _ = run_layer(inp)
+    ids, w, we, y = oracle_layer(inp, inp.logits.numpy())
+    pm = oracle.permute(ids, cfg.E, smt.numpy())
+    assert pm["n_miss"] > 0
+    assert out["n_miss"][0] == pm["n_miss"]
+    assert np.array_equal(out["miss_ids"][:pm["n_miss"]], pm["miss_ids"])
+    check_y(out["y"], y, what="random slot map")
+
+
+def test_prefill_sampled_rows():
+    """2,048-token chunk: every output row is finite; the oracle checks sampled
+    rows, including rows routed to the hottest expert, the first and the last."""
+    cfg = synth.PREFILL
+    inp = synth.make_layer(cfg, 0, device=DEV)
+    out, _ = run_layer(inp)
+    hinp = inp.to("cpu")
+    ids, w, we = oracle.route(hinp.logits.numpy(), cfg.k)
+    assert np.array_equal(out["ids"], ids)
+    assert_weights_match(out["w"], w, we)
+    assert np.all(np.isfinite(out["y"]))
+    hot = np.bincount(ids.ravel(), minlength=cfg.E).argmax()
+    rows_hot = np.nonzero((ids == hot).any(1))[0]
+    rng = np.random.default_rng(0)
+    rows = sorted(set([0, cfg.T - 1] + list(rng.choice(cfg.T, 10, replace=False)) +
+                      list(rows_hot[:3]) + list(rows_hot[-3:])))
+    y = oracle.Layer(hinp).rows(ids, w, rows=rows)
+    check_y(out["y"][rows], y, what="prefill sampled rows")
+
+
+@pytest.mark.parametrize("T", [1, 3, 5, 13, 16, 17, 33, 100])
+def test_ragged_windows(T):
+    cfg = synth.MoeConfig("rag", H=512, I=256, E=32, k=4, T=T, shared_I=256, zipf_s=1.0)
+    inp = synth.make_layer(cfg, T)
+    out, _ = run_layer(inp)
+    ids, w, we, y = oracle_layer(inp, inp.logits.numpy())
+    assert np.array_equal(out["ids"], ids)
+    check_y(out["y"], y, what=f"T={T}")
+
+
+def test_min_shapes_and_max_k():
+    cfg = synth.MoeConfig("min", H=128, I=128, E=40, k=32, T=3, shared_I=128, zipf_s=0.0)
+    inp = synth.make_layer(cfg, 2)
+    out, _ = run_layer(inp)
+    ids, w, we, y = oracle_layer(inp, inp.logits.numpy())
+    assert np.array_equal(out["ids"], ids)
+    check_y(out["y"], y, what="min shapes")
+
+
+def test_no_resident_expert_gives_shared_only():
+    cfg = synth.MoeConfig("none", H=256, I=128, E=16, k=4, T=6, shared_I=256, zipf_s=1.0)
+    inp = synth.make_layer(cfg, 3)
+    sm = torch.full((cfg.E,), -1, dtype=torch.int32)
+    out, _ = run_layer(inp, slot_map=sm)
+    ids, w, we, y = oracle_layer(inp, inp.logits.numpy(), slot_map=sm.numpy())
+    assert out["n_miss"][0] == len(set(ids.ravel().tolist()))
+    assert np.array_equal(out["miss_ids"][:out["n_miss"][0]], np.unique(ids))
+    check_y(out["y"], y, what="shared only")
+
+
+def test_empty_window_is_a_noop():
+    cfg = synth.MoeConfig("empty", H=256, I=128, E=8, k=2, T=4)
+    inp = synth.make_layer(cfg, 0).to(DEV)
+    lay = MoeLayer(inp, T_max=4)
+    out = lay.alloc_outputs(0)
+    out["n_miss"].fill_(5)
+    _lib.moe_layer_forward(lay.desc, None, None, lay.x_dtype, 0, None, out["y"], out["ids"],
+                           out["w"], out["miss_ids"], out["n_miss"], lay.ws_ptr, lay.ws_bytes)
+    torch.cuda.synchronize()
+    assert int(out["n_miss"].item()) == 0
+
+
+def test_deterministic_and_window_composition_invariant():
+    """Same inputs, same bits (run to run); and on the decode path a row's output
+    does not depend on the other rows of its window."""
+    cfg = synth.DECODE_WINDOW.with_T(16)
+    inp = synth.make_layer(cfg, 11, device=DEV)
+    out1, lay = run_layer(inp)
+    out2, _ = run_layer(inp, lay=lay)
+    assert hashlib.sha256(out1["y"].tobytes()).hexdigest() == hashlib.sha256(out2["y"].tobytes()).hexdigest()
+    for t in (0, 5, 15):
+        lg = inp.logits[t:t + 1]
+        x = inp.x[t:t + 1]
+        alone, _ = run_layer(inp, logits=lg, x=x, lay=lay)
+        assert np.array_equal(alone["y"][0], out1["y"][t]), t
+
+
+def test_launch_count_reported():
+    cfg = synth.MoeConfig("lc", H=256, I=128, E=8, k=2, T=4)
+    inp = synth.make_layer(cfg, 0)
+    run_layer(inp)
+    assert _lib.moe_last_launch_count() >= 3
