@@ -137,6 +137,26 @@ moe_status moe_layer_forward(const moe_layer_desc *L, const float *logits, const
                              int32_t *ids, float *w, int32_t *miss_ids, int32_t *n_miss,
                              void *ws, size_t ws_bytes, void *stream);
 
+/* The routed-expert FFN for callers that cannot allocate device memory. The
+ * Strata pages have no counterpart of this entry point: it exists for code
+ * that cannot obtain a workspace (inside a framework whose allocator owns all
+ * device memory, plugin code without an allocator handle, decode loops that
+ * must not call cudaMalloc). Same arguments and results as moe_expert_ffn,
+ * without ws/ws_bytes: the scratch is a fixed 16 MiB array inside the
+ * library's device memory, reserved on every GPU that loads the library until
+ * the process exits; nothing is allocated.
+ *  - Returns MOE_ERR_UNSUPPORTED when moe_workspace_bytes(L, T) exceeds
+ *    16 MiB (e.g. 2,048-token chunks): use moe_expert_ffn with a workspace.
+ *  - Every call on a device shares the array and it keeps the last call's
+ *    contents; the status word is cleared at each call. Calls that overlap on
+ *    the GPU race on it: serialise them. moe_read_status() cannot reach this
+ *    array; device-detected problems are not reported through it.
+ *  - The first call on a device looks up the array's address with that device
+ *    current; make the first call before any stream capture. */
+moe_status moe_expert_ffn_static(const moe_layer_desc *L, const void *x, moe_dtype x_dtype, int T,
+                                 const int32_t *ids, const float *w, const int32_t *slot_map,
+                                 float *y, int32_t *miss_ids, int32_t *n_miss, void *stream);
+
 /* Workspace bytes a call with this layer and T rows needs (256-byte aligned
  * base required). L is a HOST pointer. Returns 0 for an invalid desc. */
 size_t moe_workspace_bytes(const moe_layer_desc *L, int T);

@@ -22,7 +22,8 @@ MOE_F32, MOE_BF16 = 0, 1
 EXPORTS = ("moe_router_logits", "moe_route", "moe_permute", "moe_expert_ffn", "moe_layer_forward",
            "moe_workspace_bytes", "moe_workspace_init", "moe_read_status", "moe_status_str",
            "moe_last_launch_count", "moe_profile_enable", "moe_profile_collect",
-           "moe_profile_forget", "moe_profile_totals", "moe_profile_kind_name")
+           "moe_profile_forget", "moe_profile_totals", "moe_profile_kind_name",
+           "moe_expert_ffn_static")
 
 
 class MoeError(RuntimeError):
@@ -76,6 +77,7 @@ def load(path: str = LIB_PATH):
             "moe_profile_totals": ([ctypes.c_int32, ctypes.POINTER(ctypes.c_double),
                                     ctypes.POINTER(ctypes.c_int64)], i32),
             "moe_profile_kind_name": ([ctypes.c_int32], ctypes.c_char_p),
+            "moe_expert_ffn_static": ([D, P, i32, i32, P, P, P, P, P, P, P], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -132,6 +134,14 @@ def moe_expert_ffn(desc, x, x_dtype, T, ids, w, slot_map, y, miss_ids, n_miss, w
     _check("moe_expert_ffn", load().moe_expert_ffn(
         ctypes.byref(desc), _ptr(x), x_dtype, T, _ptr(ids), _ptr(w), _ptr(slot_map), _ptr(y),
         _ptr(miss_ids), _ptr(n_miss), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_expert_ffn_static(desc, x, x_dtype, T, ids, w, slot_map, y, miss_ids, n_miss, stream=None):
+    """moe_expert_ffn without a workspace argument: for callers that cannot
+    allocate device memory (the library's own fixed 16 MiB scratch is used)."""
+    _check("moe_expert_ffn_static", load().moe_expert_ffn_static(
+        ctypes.byref(desc), _ptr(x), x_dtype, T, _ptr(ids), _ptr(w), _ptr(slot_map), _ptr(y),
+        _ptr(miss_ids), _ptr(n_miss), _stream(stream)))
 
 
 def moe_layer_forward(desc, logits, x, x_dtype, T, slot_map, y, ids, w, miss_ids, n_miss, ws,
