@@ -326,10 +326,11 @@ def run_ours(args, dist):
     totals = _lib.moe_profile_totals()
     _lib.moe_profile_enable(0)
     prof_steps = [((r % len(pgraphs)) * R + i) for r in range(n_prof) for i in range(R)]
-    kb = {"gateup": 0, "down": 0}
+    kb = {"gateup": 0, "down": 0, "fused_decode": 0}
     for i in prof_steps:
         for kk, v in wl.kernel_bytes(i).items():
             kb[kk] += v
+        kb["fused_decode"] += wl.step_bytes(i)
     hbm_peak, tf_peak, tf_sus, peak_src = load_peaks()
     kern = {}
     for name, (tms, cnt) in totals.items():
@@ -338,7 +339,7 @@ def run_ours(args, dist):
     tot_ms = sum(v[0] for v in totals.values())
     for name in kern:
         kern[name]["share"] = round(totals[name][0] / tot_ms, 4) if tot_ms else None
-    dom = max(("gateup", "down"), key=lambda n: totals.get(n, (0, 0))[0])
+    dom = max(("gateup", "down", "fused_decode"), key=lambda n: totals.get(n, (0, 0))[0])
     dom_ms, dom_cnt = totals[dom]
     achieved = (kb[dom] / dom_cnt) / (dom_ms / dom_cnt * 1e-3) / 1e9
     traffic = ncu_traffic(dom, "decode_window")

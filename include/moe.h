@@ -161,8 +161,9 @@ moe_status moe_expert_ffn_static(const moe_layer_desc *L, const void *x, moe_dty
  * base required). L is a HOST pointer. Returns 0 for an invalid desc. */
 size_t moe_workspace_bytes(const moe_layer_desc *L, int T);
 
-/* Zero a workspace's status word and counters (once after allocating it, and
- * to clear a reported status). Asynchronous on stream. */
+/* Zero a workspace's status word and counters: once after allocating it, and
+ * after any call that reported a device status (a timed-out call can leave the
+ * counters non-zero). Needs ws_bytes >= 16,896. Asynchronous on stream. */
 moe_status moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* Synchronise `stream`, then read the workspace status word into *out (HOST

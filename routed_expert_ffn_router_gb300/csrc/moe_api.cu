@@ -76,6 +76,7 @@ WsLayout ws_layout(int E, int k, int T, int H, int I, int shI) {
   L.Imax = Imax;
   L.status = o;    o += 256;
   L.counters = o;  o += 256;
+  L.sync = o;      o += (size_t)kSyncInts * 4;
   L.offsets = o;   o += align256(((size_t)E + 1) * 4);
   L.sorted_pair = o; o += align256((P ? P : 1) * 4);
   L.pair_pos = o;  o += align256((P ? P : 1) * 4);
@@ -220,7 +221,7 @@ moe_status moe_profile_totals(int32_t kind, double* total_ms, int64_t* count) {
 
 const char* moe_profile_kind_name(int32_t kind) {
   static const char* names[K_NUM_KINDS] = {"router_logits", "route", "permute", "x_prep",
-                                           "gateup", "down", "combine"};
+                                           "gateup", "down", "combine", "fused_decode"};
   if (kind < 0 || kind >= K_NUM_KINDS) return "";
   return names[kind];
 }
@@ -232,8 +233,9 @@ size_t moe_workspace_bytes(const moe_layer_desc* L, int T) {
 
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   g_launches = 0;
-  if (!ws || ws_bytes < 512 || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_WORKSPACE;
-  return cuda_status(cudaMemsetAsync(ws, 0, 512, static_cast<cudaStream_t>(stream)));
+  if (!ws || ws_bytes < kWsHeadBytes || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, kWsHeadBytes, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_read_status(const void* ws, void* stream, int32_t* out) {
@@ -305,6 +307,35 @@ moe_status moe_permute(const int32_t* ids, int T, int E, int k, const int32_t* s
   return cuda_status(launch_permute(ids, T, E, k, slot_map, S, false, o, st));
 }
 
+// The one-launch decode path: routing (when logits are given), permutation,
+// gate/up, down and combine in one persistent kernel.
+static moe_status fused_impl(const moe_layer_desc* Ld, const float* logits, const void* x, int T,
+                             const int32_t* ids, const float* w, const int32_t* slot_map, float* y,
+                             int32_t* ids_out, float* w_out, int32_t* miss_ids, int32_t* n_miss,
+                             void* ws, const WsLayout& L, cudaStream_t st) {
+  FusedLaunch f{};
+  f.gq = Ld->gate.q; f.gs = Ld->gate.scale;
+  f.uq = Ld->up.q;   f.us = Ld->up.scale;
+  f.dq = Ld->down.q; f.ds = Ld->down.scale;
+  if (Ld->shared_I > 0) {
+    f.sgq = Ld->shared_gate.q; f.sgs = Ld->shared_gate.scale;
+    f.suq = Ld->shared_up.q;   f.sus = Ld->shared_up.scale;
+    f.sdq = Ld->shared_down.q; f.sds = Ld->shared_down.scale;
+  }
+  f.H = Ld->H; f.I = Ld->I; f.shI = Ld->shared_I; f.E = Ld->E; f.k = Ld->k; f.S = Ld->S;
+  f.T = T; f.Imax = L.Imax; f.rows_cap = L.P + T;
+  f.logits = logits; f.ids_in = ids; f.w_in = w;
+  f.x = x; f.slot_map = slot_map;
+  f.ids_out = ids_out; f.w_out = w_out; f.y = y; f.miss_ids = miss_ids; f.n_miss = n_miss;
+  f.hhi = at<uint16_t>(ws, L.hhi);
+  f.hlo = at<uint16_t>(ws, L.hlo);
+  f.hcorr = at<float>(ws, L.hsum);
+  f.partial = at<float>(ws, L.partial);
+  f.status = at<int32_t>(ws, L.status);
+  f.sync = at<int32_t>(ws, L.sync);
+  return cuda_status(launch_fused_decode(f, st));
+}
+
 static moe_status expert_ffn_impl(const moe_layer_desc* Ld, const void* x, moe_dtype x_dtype, int T,
                                   const int32_t* ids, const float* w, const int32_t* slot_map,
                                   float* y, int32_t* miss_ids, int32_t* n_miss, void* ws,
@@ -314,6 +345,9 @@ static moe_status expert_ffn_impl(const moe_layer_desc* Ld, const void* x, moe_d
   if (s != MOE_OK) return s;
   if (T == 0) return cuda_status(cudaMemsetAsync(n_miss, 0, sizeof(int32_t), st));
   if (!x || !ids || !w || !y || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID;
+  if (fused_decode_supported(Ld->H, Ld->I, Ld->shared_I, T, x_dtype == MOE_BF16))
+    return fused_impl(Ld, nullptr, x, T, ids, w, slot_map, y, nullptr, nullptr, miss_ids, n_miss,
+                      ws, L, st);
   const bool has_shared = Ld->shared_I > 0;
   PermuteOut o;
   o.offsets = at<int32_t>(ws, L.offsets);
@@ -387,6 +421,11 @@ moe_status moe_layer_forward(const moe_layer_desc* L, const float* logits, const
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (T == 0) return cuda_status(cudaMemsetAsync(n_miss, 0, sizeof(int32_t), st));
   if (!logits || !ids || !w) return MOE_ERR_INVALID;
+  if (fused_decode_supported(L->H, L->I, L->shared_I, T, x_dtype == MOE_BF16)) {
+    if (!x || !y || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID;
+    return fused_impl(L, logits, x, T, nullptr, nullptr, slot_map, y, ids, w, miss_ids, n_miss, ws,
+                      Lw, st);
+  }
   cudaError_t e = launch_route(logits, T, L->E, L->k, ids, w, at<int32_t>(ws, Lw.status), st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   return expert_ffn_impl(L, x, x_dtype, T, ids, w, slot_map, y, miss_ids, n_miss, ws, ws_bytes, st);

@@ -9,7 +9,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include "../../include/moe.h"
+#include "moe.h"
 
 namespace moe {
 
@@ -32,8 +32,13 @@ constexpr float kMagic = 136.0f;      // bf16 0x4300|n' = 128 + (q ^ 8) = 136 + 
 
 // ---------------------------------------------------------------- workspace
 // All offsets are 256-byte aligned. The layout depends only on (desc, T).
+// The first kWsHeadBytes hold the status word, counters and the fused kernel's
+// cross-CTA counters; moe_workspace_init zeroes exactly this head.
+constexpr size_t kWsHeadBytes = 512 + 16384;
+constexpr int kSyncInts = 4096;  // cross-CTA counters of the fused decode kernel
+
 struct WsLayout {
-  size_t status, counters, offsets, sorted_pair, pair_pos, act, cu, hist;
+  size_t status, counters, sync, offsets, sorted_pair, pair_pos, act, cu, hist;
   size_t xhi, xlo, xcorr, hhi, hlo, hsum, partial, total;
   int P, Imax, n_chunks, cu_max;
 };
@@ -136,12 +141,124 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D += A(16x16 f16, row) * B(16x8 f16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four f16x2 registers from one word of int4 codes, holding 1032 + code: the
+// nibble lands in the low mantissa bits of the f16 constant 1024 (0x6400)
+// and bit 3 is flipped (q -> q + 8). Same column order as dequant_word.
+__device__ __forceinline__ void dequant_word_f16(uint32_t w, uint32_t (&d)[4]) {
+  const uint32_t mask = 0x000F000Fu, magic = 0x64086408u;
+  d[0] = lop3_and_xor(w, mask, magic);
+  d[1] = lop3_and_xor(w >> 4, mask, magic);
+  d[2] = lop3_and_xor(w >> 8, mask, magic);
+  d[3] = lop3_and_xor(w >> 12, mask, magic);
+}
+
+// TMA tensor loads into this CTA's shared memory, completing on `bar`. The
+// innermost coordinate times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+// Byte offset inside a region written by a 128-byte-swizzled TMA box whose base
+// is 1024-byte aligned: the 16-byte chunk index is XOR-ed with the 128-byte row.
+__device__ __forceinline__ uint32_t swz128(uint32_t off) { return off ^ (((off >> 7) & 7u) << 4); }
+
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
+}
+
+// L2-only 16-byte load (bypasses L1): for data other CTAs wrote during the
+// same kernel, read after an acquire.
+__device__ __forceinline__ uint4 ldg_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ldg_cg_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Spin until *p >= target (acquire), giving up after ~1 s with DEV_TIMEOUT.
+__device__ __forceinline__ bool wait_counter_bounded(const int* p, int target, int32_t* status) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if ((it & 15) == 0 && globaltimer_ns() - t0 > 1000000000ull) {
+      if (status) atomicOr(status, DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Release-ordered atomic add at GPU scope: this thread's earlier writes, and
+// those it observed through a CTA barrier, are visible before the add.
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
 }
 
 // Position of column j (0..7) of an 8-column group in the fragment order

@@ -11,7 +11,8 @@ namespace moe {
 
 // Kernel kinds for the optional event timing (moe_profile_*).
 enum KernelKind : int {
-  K_ROUTER_LOGITS = 0, K_ROUTE, K_PERMUTE, K_X_PREP, K_GATEUP, K_DOWN, K_COMBINE, K_NUM_KINDS
+  K_ROUTER_LOGITS = 0, K_ROUTE, K_PERMUTE, K_X_PREP, K_GATEUP, K_DOWN, K_COMBINE, K_FUSED,
+  K_NUM_KINDS
 };
 
 // Every kernel launch is bracketed by these: they count launches and, when
@@ -74,5 +75,32 @@ cudaError_t launch_ffn_decode(const FfnArgs& a, const void* x, bool x_bf16, int 
                               cudaStream_t st);
 
 int cu_bound(int T, int E, int k, bool has_shared);
+
+// The one-launch decode path (moe_fused.cu).
+struct FusedLaunch {
+  const uint8_t *gq, *uq, *dq;
+  const uint16_t *gs, *us, *ds;
+  const uint8_t *sgq, *suq, *sdq;
+  const uint16_t *sgs, *sus, *sds;
+  int H, I, shI, E, k, S, T, Imax, rows_cap;
+  const float* logits;     // layer mode when non-null
+  const int32_t* ids_in;
+  const float* w_in;
+  const void* x;
+  const int32_t* slot_map;
+  int32_t* ids_out;
+  float* w_out;
+  float* y;
+  int32_t* miss_ids;
+  int32_t* n_miss;
+  uint16_t* hhi;
+  uint16_t* hlo;
+  float* hcorr;
+  float* partial;
+  int32_t* status;
+  int32_t* sync;
+};
+bool fused_decode_supported(int H, int I, int shI, int T, bool x_bf16);
+cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st);
 
 }  // namespace moe

@@ -65,8 +65,8 @@ extern "C" moe_status moe_expert_ffn_static(const moe_layer_desc* L, const void*
   void* ws = static_scratch_ptr();
   if (!ws) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the previous call's status bits must not leak into this one
-  if (cudaMemsetAsync(ws, 0, 512, st) != cudaSuccess) {
+  // the previous call's status bits and counters must not leak into this one
+  if (cudaMemsetAsync(ws, 0, moe::kWsHeadBytes, st) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }

@@ -325,3 +325,67 @@ def test_launch_count_reported():
     inp = synth.make_layer(cfg, 0)
     run_layer(inp)
     assert _lib.moe_last_launch_count() >= 3
+
+
+# ---------------------------------------------------------------- one-launch decode path
+def test_fused_all_missing_without_shared_gives_zero():
+    cfg = synth.MoeConfig("f0", H=512, I=256, E=16, k=4, T=6, zipf_s=1.0)
+    inp = synth.make_layer(cfg, 3)
+    sm = torch.full((cfg.E,), -1, dtype=torch.int32)
+    out, _ = run_layer(inp, slot_map=sm)
+    assert np.all(out["y"] == 0)
+    ids, _, _ = oracle.route(inp.logits.numpy(), cfg.k)
+    assert out["n_miss"][0] == len(np.unique(ids))
+
+
+def test_fused_no_resident_expert_gives_shared_only():
+    cfg = synth.MoeConfig("f1", H=512, I=256, E=16, k=4, T=6, shared_I=512, zipf_s=1.0)
+    inp = synth.make_layer(cfg, 4)
+    sm = torch.full((cfg.E,), -1, dtype=torch.int32)
+    out, _ = run_layer(inp, slot_map=sm)
+    ids, w, we, y = oracle_layer(inp, inp.logits.numpy(), slot_map=sm.numpy())
+    check_y(out["y"], y, what="fused shared only")
+
+
+def test_fused_ffn_mode_matches_layer_mode_and_repeats():
+    """moe_expert_ffn (routing given) and moe_layer_forward agree bit for bit, and
+    repeated calls on one workspace give the same bits (counters reset)."""
+    cfg = synth.MoeConfig("f2", H=2048, I=768, E=128, k=8, T=12, shared_I=768, zipf_s=1.1)
+    inp = synth.make_layer(cfg, 8, device=DEV)
+    out1, lay = run_layer(inp)
+    ids = torch.from_numpy(out1["ids"]).to(DEV)
+    w = torch.from_numpy(out1["w"]).to(DEV)
+    for _ in range(3):
+        o2 = lay.expert_ffn(inp.x, ids, w)
+        torch.cuda.synchronize()
+        assert np.array_equal(o2["y"].cpu().numpy(), out1["y"])
+        out3, _ = run_layer(inp, lay=lay)
+        assert np.array_equal(out3["y"], out1["y"])
+    code, bits = lay.status()
+    assert code == _lib.MOE_OK, bits
+
+
+def test_fused_window_sizes_share_one_workspace():
+    cfg = synth.MoeConfig("f3", H=1024, I=512, E=64, k=6, T=16, shared_I=256, zipf_s=1.0)
+    inp = synth.make_layer(cfg, 12, device=DEV)
+    lay = MoeLayer(inp, T_max=16)
+    hinp = inp.to("cpu")
+    for T in (16, 1, 7, 16, 3):
+        out, _ = run_layer(inp, logits=inp.logits[:T], x=inp.x[:T], lay=lay)
+        ids, w, _ = oracle.route(hinp.logits[:T].numpy(), cfg.k)
+        y = oracle.Layer(hinp).rows(ids, w)
+        check_y(out["y"], y, what=f"T={T}")
+
+
+def test_fused_flags_non_finite_logit():
+    cfg = synth.MoeConfig("f4", H=512, I=256, E=16, k=4, T=4, zipf_s=1.0)
+    inp = synth.make_layer(cfg, 1).to(DEV)
+    lay = MoeLayer(inp, T_max=4)
+    lg = inp.logits.clone()
+    lg[1, 3] = float("nan")
+    lay.forward(lg, inp.x)
+    code, bits = lay.status()
+    assert code == _lib.MOE_ERR_DEVICE and bits & 1
+    lay.clear_status()
+    lay.forward(inp.logits, inp.x)
+    assert lay.status()[0] == _lib.MOE_OK
