@@ -92,7 +92,15 @@ WsLayout ws_layout(int E, int k, int T, int H, int I, int shI) {
   L.hhi = o;       o += align256(rows * Imax * 2);
   L.hlo = o;       o += align256(rows * Imax * 2);
   L.hsum = o;      o += align256(rows * (Imax / 16) * 4);
-  L.partial = o;   o += align256(rows * (size_t)H * 4);
+  // The one-launch decode path keeps one partial per slice of I; a smaller
+  // window may cut I finer, and a workspace sized for T serves every T' <= T.
+  size_t prow = rows;
+  for (int t = 1; t <= T && t <= 16; ++t) {
+    const size_t r = (size_t)t * k + t;
+    const size_t n = r * (size_t)fused_partial_slices(E, k, t, I, shI);
+    prow = n > prow ? n : prow;
+  }
+  L.partial = o;   o += align256(prow * (size_t)H * 4);
   L.total = o;
   return L;
 }

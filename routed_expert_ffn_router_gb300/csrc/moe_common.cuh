@@ -83,17 +83,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
+// Time bound of every wait: about a second of SM clock cycles. The SM's own
+// cycle counter is read in a few cycles (the global timer takes far longer),
+// so a wait costs nothing when it does not have to wait.
+constexpr long long kWaitCycles = 2000000000ll;
+__device__ __forceinline__ long long cycles_now() { return clock64(); }
 
-// Wait for phase `parity` of `bar`, giving up after ~1 s: then the status word
-// gets DEV_TIMEOUT and the caller skips its work. Returns true on success.
+// Wait for phase `parity` of `bar`, giving up after about a second: then the
+// status word gets DEV_TIMEOUT and the caller skips its work. Returns true on success.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   int32_t* status) {
-  uint64_t t0 = 0;
+  long long t0 = 0;
   for (uint32_t it = 0;; ++it) {
     uint32_t ok;
     asm volatile(
@@ -102,12 +102,55 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
         : "r"(bar), "r"(parity)
         : "memory");
     if (ok) return true;
-    if (it == 0) t0 = globaltimer_ns();
-    else if ((it & 63) == 0 && globaltimer_ns() - t0 > 1000000000ull) {
+    if (it == 0) t0 = cycles_now();
+    else if ((it & 63) == 0 && cycles_now() - t0 > kWaitCycles) {
       if (status) atomicOr(status, DEV_TIMEOUT);
       return false;
     }
   }
+}
+
+// Non-blocking test of phase `parity` of `bar` (true once that phase completed).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// 4-byte asynchronous copy global -> shared (completes at cp_async_wait_all).
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Fetch a TMA descriptor (kernel parameter) ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// Programmatic dependent launch: let the stream's next kernel be scheduled;
+// wait until the stream's previous kernel has completed (and its writes are visible).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Wait (suspended, up to about `ns` nanoseconds) for phase `parity` of `bar`;
+// true once that phase completed. Leaves the issue slots to the other warps.
+__device__ __forceinline__ bool mbar_try_wait_ns(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
 }
 
 // f = (a & b) ^ c
@@ -134,7 +177,7 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&d)[4]) {
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
                                                uint32_t a2, uint32_t a3, uint32_t b0,
                                                uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -145,7 +188,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
                                               uint32_t a2, uint32_t a3, uint32_t b0,
                                               uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -182,6 +225,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// L2 policy for data read once per call (the expert weights): evicted before
+// anything else, so the stream does not push the kernel's code and the small
+// per-call buffers out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap, int c0, int c1,
+                                                 uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+          dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // Byte offset inside a region written by a 128-byte-swizzled TMA box whose base
 // is 1024-byte aligned: the 16-byte chunk index is XOR-ed with the 128-byte row.
 __device__ __forceinline__ uint32_t swz128(uint32_t off) { return off ^ (((off >> 7) & 7u) << 4); }
@@ -192,6 +252,23 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
 
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Shared-memory loads by 32-bit shared-window address.
+__device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 ld_s128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float ld_s_half_as_float(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(a));
+  return __half2float(__ushort_as_half(v));
 }
 
 __device__ __forceinline__ uint4 lds_v4(const void* p) {
@@ -226,14 +303,14 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   return v;
 }
 
-// Spin until *p >= target (acquire), giving up after ~1 s with DEV_TIMEOUT.
+// Spin until *p >= target (acquire), giving up after about a second with DEV_TIMEOUT.
 __device__ __forceinline__ bool wait_counter_bounded(const int* p, int target, int32_t* status) {
   if (ld_acquire_gpu(p) >= target) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = cycles_now();
   for (uint32_t it = 1;; ++it) {
     __nanosleep(64);
     if (ld_acquire_gpu(p) >= target) return true;
-    if ((it & 15) == 0 && globaltimer_ns() - t0 > 1000000000ull) {
+    if ((it & 15) == 0 && cycles_now() - t0 > kWaitCycles) {
       if (status) atomicOr(status, DEV_TIMEOUT);
       return false;
     }

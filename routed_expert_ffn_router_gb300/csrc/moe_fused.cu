@@ -4,27 +4,31 @@
 // This is the grouped expert call of the SGLang port post (TL;DR and section
 // 3: gather -> dequant -> gate/up -> SwiGLU -> down -> scatter in one call per
 // layer) laid out for GB300:
-//  * one CTA per SM; warp 0 streams jobs into a ring of shared-memory stages
-//    with TMA tensor copies (full/empty mbarriers). A job is a tile of packed
-//    weight rows (int4 codes in 128-byte-swizzled tiles, fp16 scales) together
-//    with the activation rows it multiplies (a chunk of x, or the expert's
-//    chunk of h): a handful of copies per job, and the 8 consumer warps never
-//    wait on global memory. They split the job's columns and run the
-//    exact-integer warp-MMA core (moe_decode.cu explains the 136 + q and
-//    1032 + q code fragments);
-//  * the per-block correction -magic * sum(B) comes from one more MMA whose A
-//    operand is the constant -magic;
+//  * one CTA per SM. Warp 0 (one thread) is the producer: it takes work units
+//    from a grid-wide queue (one atomic per unit) and streams each unit's jobs
+//    into a ring of shared-memory stages with TMA tensor copies (full/empty
+//    mbarriers; the weights with an evict-first L2 policy). It also publishes
+//    finished units, so no consumer waits on a gpu-scope fence;
+//  * a unit is UI = 32 MT intermediate rows of one expert: its gate/up rows
+//    over all of H (H / 256 jobs), then that slice of I's contribution to the
+//    down projection (H / 256 jobs of 256 output rows). h never leaves the SM
+//    and no unit waits for another CTA: the units stream back to back;
+//  * the 8 consumer warps are 4 row warps x 2 column halves for gate/up (row
+//    warp mw owns MT m16 tiles, half kh sums blocks 4kh..4kh+3 of each
+//    256-column chunk) and 8 row warps for down. A row's summation order
+//    depends only on H and I, never on the window;
+//  * gate/up tiles interleave 8 gate rows and the same 8 up rows, so an MMA
+//    accumulator holds g and u of one intermediate index side by side and
+//    SwiGLU happens in registers; h is kept as fp16 in the down operand's
+//    fragment order. The exact-integer warp-MMA core (moe_decode.cu explains
+//    the 136 + q and 1032 + q code fragments) gets its per-block correction
+//    -magic * sum(B) from one more MMA whose A operand is the constant -magic;
 //  * every CTA computes the top-k ids and the permutation of the whole window
 //    in shared memory, so no launch precedes the weight stream; CTA t computes
 //    row t's float64 softmax weights;
-//  * phase 1: gate/up units (32 rows of gate and of up, K in chunks), handed
-//    out round-robin, write h = silu(g)*u as fp16 in fragment order; phase 2:
-//    down units (R output rows, contiguous per CTA). The producer issues a
-//    down job's weight copies at once and its h copy after the expert's
-//    gate/up units are all done (a per-expert counter);
-//  * the last CTA to finish a group of R output rows sums the routed partials
-//    in j order, weighted, then adds the shared expert: y is deterministic;
-//  * the last CTA to exit resets the cross-CTA counters for the next call.
+//  * once every unit is published, the CTAs share the reduction
+//    y = sum_j w_j sum_g p(e_j, g) + sum_g p(shared, g) in a fixed order, so y is
+//    deterministic; the last CTA to exit resets the cross-CTA counters.
 // Every expert a window touches (and the shared expert, Strata BATCHING,
 // "Several requests at once") is read from HBM exactly once.
 #include <cuda.h>
@@ -40,20 +44,23 @@
 namespace moe {
 namespace fused {
 
-constexpr int kCW = 8;                  // consumer warps
+constexpr int kCW = 8;                  // consumer warps: 4 row warps x 2 column halves
 constexpr int kThreads = 32 * (kCW + 1);
-constexpr int kNst = 4;                 // pipeline stages
-constexpr int kGuRows = 32;             // rows of gate and of up per unit (one block of I)
-constexpr int kMaxT = 16;               // largest window; x / h boxes hold TB = 8 or 16 rows
-constexpr int kMaxMT = 4;               // m16 tiles per job
-constexpr int kRed = 8 * 17;            // one (m-tile, n-tile) slab: 8 tokens x (16 rows + pad)
-constexpr int kRedBytes = kCW * kMaxMT * 2 * kRed * 4;
-constexpr int kChunkE = 4;              // experts per thread in the permutation scan
+constexpr int kKC = 256;                // columns of K per job
+constexpr int kMaxNst = 8;              // stages in the ring at most
+constexpr int kUnitRing = 16;           // units a producer may have unpublished
+constexpr int kMaxT = 16;               // largest window; x boxes hold TB = 8 or 16 rows
+constexpr int kDnRows = 512;            // output rows per down job (two 256-row boxes)
+constexpr int kDnM = kDnRows / (kCW * 16);  // m16 tiles per warp in a down job
+constexpr int kPubCount = kCW * 32;     // arrivals that publish a unit (every consumer lane)
+constexpr int kPubBars = 4;             // publish barriers, used by units in turn
 constexpr uint32_t kBf16NegMagic = 0xC308C308u;  // bf16 -136
 constexpr uint32_t kF16NegMagic = 0xE408E408u;   // f16 -1032
 
 // cross-CTA counters (int32 offsets in the workspace sync region)
-constexpr int kSyncDone = 0, kSyncWReady = 1, kSyncReady = 16, kSyncRg = 16 + 1040;
+constexpr int kSyncDone = 0, kSyncUnits = 1, kSyncQueue = 2;
+
+enum JobKind : int { J_GU = 0, J_DN = 1, J_END = 2 };
 
 struct Args {
   // TMA tensor maps (kernel parameters, read through their parameter address)
@@ -61,15 +68,13 @@ struct Args {
   CUtensorMap tm_gs, tm_us, tm_ds;     // routed scales
   CUtensorMap tm_sgc, tm_suc, tm_sdc;  // shared expert codes
   CUtensorMap tm_sgs, tm_sus, tm_sds;  // shared expert scales
-  CUtensorMap tm_x;                    // x [T][H] bf16, 3D box (64, KC/64, 16)
-  CUtensorMap tm_h, tm_hs;             // h [rows_cap][Imax] f16: routed / shared chunk boxes
-  int H, I, shI, E, k, S, T, Imax;
-  int KC;          // gate/up K chunk (columns per job)
-  int KCd, KCds;   // down K chunk of the routed / shared experts
-  int R;           // output rows per down unit
-  int stage_bytes; // multiple of 1024
+  CUtensorMap tm_x;                    // x [T][H] bf16, 3D box (64, 4, TB)
+  int H, I, shI, E, k, S, T;
+  int Gmax;        // slices of I per partial row (max(I, shared I) / UI)
   int TB;          // rows of the x / h boxes (8 or 16, >= T)
-  int rows_cap;    // rows of the h / partial buffers (P + T)
+  int nst;         // stages in the ring
+  int stage_bytes; // multiple of 1024
+  int rows_cap;    // rows of the partial buffer (P + T)
   const float* logits;     // non-null: route here (layer mode)
   const int32_t* ids_in;   // routing given (ffn mode)
   const float* w_in;
@@ -79,31 +84,29 @@ struct Args {
   float* y;
   int32_t* miss_ids;
   int32_t* n_miss;
-  uint16_t* h;             // f16 bits [rows_cap][Imax], fragment order
-  float* partial;          // [rows_cap][H]
+  float* partial;          // [rows_cap][Gmax][H]: one down partial per routed pair and slice
   int32_t* status;
   int32_t* sync;
 };
 
-// Dynamic shared memory: 1 KB of alignment slack, kNst stages, the cross-warp
-// reduction buffer, barriers.
-__host__ __device__ inline size_t smem_bytes(int stage_bytes) {
-  return 1024 + (size_t)kNst * stage_bytes + kRedBytes + 2 * kNst * 8;
+// Stage layouts (byte offsets from the 1024-aligned stage base), UI = 32 MT:
+//  gate/up: gate codes [UI][128 B] (swizzled), up codes [UI][128 B], x box
+//           [TB][4][128 B] (swizzled), gate scales [UI][8], up scales [UI][8];
+//  down:    codes [512][UI/2 B] (swizzled for UI/2 = 64 or 32 bytes), scales
+//           [512][8] (the 8 blocks around the unit's UI columns).
+__host__ __device__ constexpr int gu_job_bytes(int MT, int TB) { return 288 * 32 * MT + 512 * TB; }
+__host__ __device__ constexpr int dn_job_bytes(int MT) { return kDnRows * 16 * MT + 16 * kDnRows; }
+__host__ __device__ constexpr int stage_bytes_for(int MT, int TB) {
+  return gu_job_bytes(MT, TB) > dn_job_bytes(MT) ? gu_job_bytes(MT, TB) : dn_job_bytes(MT);
 }
-
-// Job stage layouts (byte offsets from the 1024-aligned stage base).
-// gate/up: gate code tiles [KC/256][32 rows][128 B] (swizzled), up code tiles,
-//          x box [TB rows][KC/64][128 B] (swizzled), gate scales [32][KC/32],
-//          up scales [32][KC/32].
-// down:    code tiles [KCd/256][R][128 B] (swizzled), h box [TB][KCd/64][128 B]
-//          (swizzled), scales [R][KCd/32].
-__host__ __device__ inline int gu_codes_bytes(int KC) { return (KC / 256) * kGuRows * 128; }
-__host__ __device__ inline int gu_x(int KC) { return 2 * gu_codes_bytes(KC); }
-__host__ __device__ inline int gu_scales(int KC, int TB) { return gu_x(KC) + TB * KC * 2; }
-__host__ __device__ inline int gu_bytes(int KC, int TB) { return gu_scales(KC, TB) + 2 * kGuRows * (KC / 16); }
-__host__ __device__ inline int dn_h(int R, int KCd) { return (KCd / 256) * R * 128; }
-__host__ __device__ inline int dn_scales(int R, int KCd, int TB) { return dn_h(R, KCd) + TB * KCd * 2; }
-__host__ __device__ inline int dn_bytes(int R, int KCd, int TB) { return dn_scales(R, KCd, TB) + R * (KCd / 16); }
+__host__ __device__ constexpr int red_bytes(int MT) { return 4 * (MT * 2 * 4) * 32 * 4; }
+// two h buffers [kMaxT][UI + 8] f16 (the 16-byte pad keeps the B loads free of bank conflicts)
+__host__ __device__ constexpr int hb_bytes(int MT) { return 2 * kMaxT * (64 * MT + 16); }
+// Dynamic shared memory: 1 KB of alignment slack, the stages, the exchange
+// buffer of the two column halves, the h buffers.
+__host__ __device__ inline size_t smem_bytes(int MT, int nst, int stage_bytes) {
+  return 1024 + (size_t)nst * stage_bytes + red_bytes(MT) + hb_bytes(MT);
+}
 
 __device__ __forceinline__ uint32_t order_key(float v) {
   uint32_t u = __float_as_uint(v);
@@ -119,35 +122,6 @@ __device__ __forceinline__ int nth_bit(uint32_t m, int n) {
   for (int i = 0; i < n; ++i) m &= m - 1;
   return __ffs(m) - 1;
 }
-
-// Exclusive scan over all kThreads threads (unsigned: packed fields may use bit 31).
-__device__ __forceinline__ uint32_t cta_excl_scan(uint32_t v, uint32_t* s_warp, uint32_t* s_total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t wv = lane < kCW + 1 ? s_warp[lane] : 0u;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      uint32_t y = __shfl_up_sync(0xffffffffu, wv, off);
-      if (lane >= off) wv += y;
-    }
-    if (lane < kCW + 1) s_warp[lane] = wv;
-    if (lane == kCW) *s_total = wv;
-  }
-  __syncthreads();
-  const uint32_t base = warp > 0 ? s_warp[warp - 1] : 0u;
-  const uint32_t r = base + x - v;
-  __syncthreads();
-  return r;
-}
-
 
 // Top-k of one row by one warp. Keys are 64-bit (order_key(logit) << 32 | ~id):
 // unique, and larger means "earlier" (logit descending, ties to the lower id).
@@ -241,50 +215,46 @@ __device__ bool topk_row(const float* l, int E, int k, unsigned long long* scr, 
 }
 
 
-// One job's columns [b0, b1) (blocks of 32) for one consumer warp:
+// One job's share for one consumer warp (row warp mw, column half kh):
 //   acc[m][nt] += sum_b scale(row, b) * (codes(row, b) . B(b, token slot))
-// GU: gate/up job (bf16 x, 136 + q codes, m-tiles 0,1 gate / 2,3 up);
-// otherwise a down job (f16 h, 1032 + q codes). All shared-memory loads of a
-// block are issued before its arithmetic, so the MT x NT MMA chains overlap.
-// Blocks b = cw, cw + 8, ... of the job: the blocks a warp sums, and their
-// order, do not depend on how K is cut into chunks.
+// over blocks b = 4 kh .. 4 kh + 3 of the stage's 256-column chunk. All
+// shared-memory loads of a block are issued before its arithmetic, so the
+// MT x NT MMA chains overlap.
+// GU: gate/up job (bf16 x, 136 + q codes); m-tile m holds gate rows
+// 8 (mw MT + m) + 0..7 of the unit in A rows 0-7 and the same up rows in A
+// rows 8-15. Otherwise a down job (f16 h, 1032 + q codes); m-tile m holds rows
+// 16 (mw MT + m) + 0..15.
 template <bool GU, int MT, int NT>
-__device__ __forceinline__ void job_compute(const uint8_t* st, int kcols, int R, int TB, int cw,
-                                            const int (&brow)[2], float (&acc)[kMaxMT][2][4]) {
+__device__ __forceinline__ void job_compute(uint32_t st, int mw, int kh, int TB,
+                                            const int (&brow)[2], float (&acc)[MT][2][4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  const int brow_bytes = kcols * 2;
-  const uint8_t* bbox = st + (GU ? gu_x(kcols) : dn_h(R, kcols));
-  const __half* scl =
-      reinterpret_cast<const __half*>(st + (GU ? gu_scales(kcols, TB) : dn_scales(R, kcols, TB)));
-  const int NB = kcols / 32;
-  const int code_tile = (GU ? kGuRows : R) * 128;
-  const int lines = kcols / 256;
+  constexpr int UI = 32 * MT, R = 64 * MT;
+  const uint32_t bbox = st + (GU ? 2 * UI * 128 : R * 128);
+  const uint32_t scl0 = bbox + TB * 512;
+  // the second code row of a lane: the up tile (gate/up), 8 rows further (down)
+  constexpr int kRow2 = GU ? UI * 128 : 8 * 128;
+  constexpr int kScl2 = GU ? UI * 16 : 8 * 16;
   // every row this lane reads is g (mod 8): one swizzle for all of them
-  const uint8_t* rowp[MT];
-  const __half* sclp[MT];
+  const int r0 = GU ? 8 * mw * MT + g : 16 * mw * MT + g;
+  const uint32_t rowp = st + r0 * 128 + c * 4;
+  const uint32_t sclp = scl0 + r0 * 16;
+  constexpr int kMStep = GU ? 8 : 16;  // rows between m-tiles
 #pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    const int mat = GU ? (m >> 1) : 0;
-    const int r0 = GU ? (m & 1) * 16 + g : m * 16 + g;
-    rowp[m] = st + (size_t)mat * lines * code_tile + r0 * 128 + c * 4;
-    sclp[m] = scl + ((GU ? mat * kGuRows : 0) + r0) * NB;
-  }
-#pragma unroll 1
-  for (int b = cw; b < NB; b += kCW) {
-    const int line = b >> 3, chunk = b & 7;
+  for (int i = 0; i < 4; ++i) {
+    const int b = kh * 4 + i;
     uint4 braw[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
-      braw[nt] = lds_v4(bbox + swz128((uint32_t)(brow[nt] * brow_bytes + b * 64 + c * 16)));
-    const int coff = line * code_tile + ((chunk ^ g) << 4);
+      braw[nt] = ld_s128(bbox + swz128((uint32_t)(brow[nt] * 512 + b * 64 + c * 16)));
+    const int coff = (b ^ g) << 4;
     uint32_t w[MT][2];
     float sc[MT][2];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      w[m][0] = *reinterpret_cast<const uint32_t*>(rowp[m] + coff);
-      w[m][1] = *reinterpret_cast<const uint32_t*>(rowp[m] + coff + 8 * 128);
-      sc[m][0] = __half2float(sclp[m][b]);
-      sc[m][1] = __half2float(sclp[m][8 * NB + b]);
+      w[m][0] = ld_s32(rowp + m * kMStep * 128 + coff);
+      w[m][1] = ld_s32(rowp + m * kMStep * 128 + kRow2 + coff);
+      sc[m][0] = ld_s_half_as_float(sclp + m * kMStep * 16 + 2 * b);
+      sc[m][1] = ld_s_half_as_float(sclp + m * kMStep * 16 + kScl2 + 2 * b);
     }
     uint32_t bf[NT][4];
     float corr[NT][4];
@@ -299,7 +269,7 @@ __device__ __forceinline__ void job_compute(const uint8_t* st, int kcols, int R,
         bf[nt][0] = braw[nt].x; bf[nt][1] = braw[nt].y; bf[nt][2] = braw[nt].z; bf[nt][3] = braw[nt].w;
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) corr[nt][i] = 0.f;
+      for (int q = 0; q < 4; ++q) corr[nt][q] = 0.f;
       if (GU) {
         mma_bf16_16816(corr[nt], kBf16NegMagic, kBf16NegMagic, kBf16NegMagic, kBf16NegMagic, bf[nt][0], bf[nt][1]);
         mma_bf16_16816(corr[nt], kBf16NegMagic, kBf16NegMagic, kBf16NegMagic, kBf16NegMagic, bf[nt][2], bf[nt][3]);
@@ -337,64 +307,186 @@ __device__ __forceinline__ void job_compute(const uint8_t* st, int kcols, int R,
   }
 }
 
-struct Job {
-  bool gu;        // gate/up (true) or down
-  int d;          // active-expert index (D = the shared expert)
-  int tile;       // gate/up: 32-row tile of I; down: R-row group of H
-  int kc;         // K chunk
-  bool first, last;
-};
-
-struct Plan {
-  int nGu;        // gate/up units of this CTA (u = bid + i*G)
-  int nKc, nKd;   // chunks per gate/up / down unit
-  int v0, v1;     // down units of this CTA
-  int nIu, D, nRg;
-  __device__ int njobs() const { return nGu * nKc + (v1 - v0) * nKd; }
-};
-
-__device__ __forceinline__ Job decode_job(int j, const Plan& p, int bid, int G) {
-  Job jb;
-  if (j < p.nGu * p.nKc) {
-    const int u = bid + (j / p.nKc) * G;
-    jb.gu = true;
-    jb.kc = j % p.nKc;
-    if (u < p.D * p.nIu) {
-      jb.d = u / p.nIu;
-      jb.tile = u - jb.d * p.nIu;
-    } else {
-      jb.d = p.D;
-      jb.tile = u - p.D * p.nIu;
-    }
-    jb.first = jb.kc == 0;
-    jb.last = jb.kc == p.nKc - 1;
-  } else {
-    const int jj = j - p.nGu * p.nKc;
-    const int v = p.v0 + jj / p.nKd;
-    jb.gu = false;
-    jb.kc = jj % p.nKd;
-    jb.d = v / p.nRg;
-    jb.tile = v - jb.d * p.nRg;
-    jb.first = jb.kc == 0;
-    jb.last = jb.kc == p.nKd - 1;
-  }
-  return jb;
+__device__ __forceinline__ float4 ldg_cg_f4(const float* p) {
+  const uint4 v = ldg_cg_v4(p);
+  return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                     __uint_as_float(v.w));
 }
 
+// One down job for one consumer warp: rows 64 cw + 16 m + (g, g + 8), m < 4,
+// of the job's 512 output rows, over the unit's UI columns of I (MT blocks):
+//   acc[m][nt] += sum_b scale(row, b) * (codes(row, b) . h(b, token slot))
+// Codes: [512][UI/2 B] with the TMA swizzle of that row width (64-, 32-byte or
+// none); scales [512][8] (the unit's blocks start at boff); h comes from the
+// unit's shared-memory buffer [slot][UI + 8] f16 in fragment order.
+template <int MT, int NT>
+__device__ __forceinline__ void dn_compute(uint32_t st, uint32_t hb, int cw, int boff,
+                                           const int (&brow)[2], float (&acc)[kDnM][2][4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  constexpr int UI = 32 * MT, RB = UI / 2;
+  constexpr uint32_t kSwz = MT == 4 ? 3u : (MT == 2 ? 1u : 0u);
+  constexpr int HB = UI * 2 + 16;
+  const uint32_t scl = st + kDnRows * RB;
+#pragma unroll
+  for (int b = 0; b < MT; ++b) {
+    uint32_t bf[NT][4];
+    float corr[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint4 v = ld_s128(hb + brow[nt] * HB + b * 64 + c * 16);
+      bf[nt][0] = v.x; bf[nt][1] = v.y; bf[nt][2] = v.z; bf[nt][3] = v.w;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) corr[nt][q] = 0.f;
+      mma_f16_16816(corr[nt], kF16NegMagic, kF16NegMagic, kF16NegMagic, kF16NegMagic, bf[nt][0], bf[nt][1]);
+      mma_f16_16816(corr[nt], kF16NegMagic, kF16NegMagic, kF16NegMagic, kF16NegMagic, bf[nt][2], bf[nt][3]);
+    }
+    uint32_t w[kDnM][2];
+    float sc[kDnM][2];
+#pragma unroll
+    for (int m = 0; m < kDnM; ++m) {
+      const int r = 16 * (kDnM * cw + m) + g;
+      const uint32_t o0 = r * RB + b * 16 + c * 4, o1 = o0 + 8 * RB;
+      w[m][0] = ld_s32(st + (o0 ^ (((o0 >> 7) & kSwz) << 4)));
+      w[m][1] = ld_s32(st + (o1 ^ (((o1 >> 7) & kSwz) << 4)));
+      sc[m][0] = ld_s_half_as_float(scl + r * 16 + 2 * (boff + b));
+      sc[m][1] = ld_s_half_as_float(scl + (r + 8) * 16 + 2 * (boff + b));
+    }
+#pragma unroll
+    for (int m = 0; m < kDnM; ++m) {
+      uint32_t d[4], e[4];
+      dequant_word_f16(w[m][0], d);
+      dequant_word_f16(w[m][1], e);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float t4[4] = {corr[nt][0], corr[nt][1], corr[nt][2], corr[nt][3]};
+        mma_f16_16816(t4, d[0], e[0], d[1], e[1], bf[nt][0], bf[nt][1]);
+        mma_f16_16816(t4, d[2], e[2], d[3], e[3], bf[nt][2], bf[nt][3]);
+        acc[m][nt][0] = fmaf(sc[m][0], t4[0], acc[m][nt][0]);
+        acc[m][nt][1] = fmaf(sc[m][0], t4[1], acc[m][nt][1]);
+        acc[m][nt][2] = fmaf(sc[m][1], t4[2], acc[m][nt][2]);
+        acc[m][nt][3] = fmaf(sc[m][1], t4[3], acc[m][nt][3]);
+      }
+    }
+  }
+}
+
+// The units of a window, in queue order: the shared expert's, then the routed
+// experts' (expert order). Unit (d, g) is intermediate rows [g UI, g UI + UI)
+// of expert d: its gate/up (H / 256 jobs) and that slice's share of the down
+// projection (H / 256 jobs of 256 output rows).
+struct Sched {
+  int D;      // resident routed experts of the window (the shared expert is d = D)
+  int nGs;    // units of the shared expert (0 without one)
+  int nGi;    // units per routed expert
+  int total;  // units in all
+  __device__ int2 unit(int t) const {  // (d, g)
+    if (t < nGs) return make_int2(D, t);
+    const int d = (t - nGs) / nGi;
+    return make_int2(d, t - nGs - d * nGi);
+  }
+};
+
+// The producer thread's state and steps (always inlined: no call may make it
+// wait for an atomic whose result it does not need yet).
+template <int MT>
+struct Producer {
+  const Args& a;
+  uint32_t sbase, full0, empty0, pub0;
+  int4* hdr;
+  const int32_t* act_slot;
+  int D;
+  uint64_t wpol;   // L2 policy of the weight copies
+  int j;           // jobs issued
+  int ui, pd;      // units taken, units published
+
+  // Publish the units whose partials are all stored (never blocks).
+  __device__ __forceinline__ void poll() {
+    while (pd < ui && mbar_test(pub0 + 8 * (pd % kPubBars), (pd / kPubBars) & 1)) {
+      __threadfence();  // the consumers' partial stores, then the count
+      atomicAdd(a.sync + kSyncUnits, 1);
+      ++pd;
+    }
+  }
+  __device__ __forceinline__ bool timed_out(long long t0) {
+    if (cycles_now() - t0 <= kWaitCycles) return false;
+    atomicOr(a.status, DEV_TIMEOUT);
+    return true;
+  }
+  // Free slot for job j (publishing meanwhile).
+  // The thread sleeps in the barrier wait between polls: a spinning producer
+  // would take issue slots from the consumer warps of its SM sub-partition.
+  __device__ __forceinline__ bool acquire_slot(int& slot) {
+    slot = j % a.nst;
+    const uint32_t par = ((j / a.nst) & 1) ^ 1;
+    if (mbar_test(empty0 + 8 * slot, par)) return true;
+    const long long t0 = cycles_now();
+    for (uint32_t it = 1;; ++it) {
+      poll();
+      if (mbar_try_wait_ns(empty0 + 8 * slot, par, 400)) return true;
+      if ((it & 15) == 0 && timed_out(t0)) return false;
+    }
+  }
+  // Sleep until the oldest unpublished unit's epilogue is done (or ~ns).
+  __device__ __forceinline__ void wait_pub(uint32_t ns) {
+    if (pd < ui) mbar_try_wait_ns(pub0 + 8 * (pd % kPubBars), (pd / kPubBars) & 1, ns);
+  }
+  __device__ __forceinline__ bool issue(int kind, int d, int grp, int chunk) {
+    constexpr int UI = 32 * MT;
+    poll();
+    int slot;
+    if (!acquire_slot(slot)) return false;
+    hdr[slot] = make_int4(kind, d, grp, chunk);
+    const uint32_t st = sbase + slot * a.stage_bytes, fb = full0 + 8 * slot;
+    ++j;
+    if (kind == J_END) {
+      mbar_arrive(fb);
+      return true;
+    }
+    const bool sh = d == D;
+    const int slotp = sh ? 0 : act_slot[d];
+    if (kind == J_GU) {
+      mbar_expect_tx(fb, (uint32_t)gu_job_bytes(MT, a.TB));
+      const int row = (sh ? 0 : slotp * a.I) + grp * UI;
+      tma_load_2d_hint(st, sh ? &a.tm_sgc : &a.tm_gc, chunk * 128, row, fb, wpol);
+      tma_load_2d_hint(st + UI * 128, sh ? &a.tm_suc : &a.tm_uc, chunk * 128, row, fb, wpol);
+      tma_load_3d(st + 2 * UI * 128, &a.tm_x, 0, chunk * 4, 0, fb);
+      const uint32_t so = st + 2 * UI * 128 + a.TB * 512;
+      tma_load_2d_hint(so, sh ? &a.tm_sgs : &a.tm_gs, chunk * 8, row, fb, wpol);
+      tma_load_2d_hint(so + UI * 16, sh ? &a.tm_sus : &a.tm_us, chunk * 8, row, fb, wpol);
+    } else {
+      mbar_expect_tx(fb, (uint32_t)dn_job_bytes(MT));
+      const int row = (sh ? 0 : slotp * a.H) + chunk * kDnRows;
+      const uint32_t so = st + kDnRows * (UI / 2);
+#pragma unroll
+      for (int h2 = 0; h2 < kDnRows / 256; ++h2) {  // boxes of 256 rows
+        tma_load_2d_hint(st + h2 * 256 * (UI / 2), sh ? &a.tm_sdc : &a.tm_dc, grp * (UI / 2),
+                         row + 256 * h2, fb, wpol);
+        tma_load_2d_hint(so + h2 * 256 * 16, sh ? &a.tm_sds : &a.tm_ds, (grp * MT) & ~7,
+                         row + 256 * h2, fb, wpol);
+      }
+    }
+    return true;
+  }
+};
+
+// MAXNT: n8 token tiles at most (1 for windows of up to 8 rows, 2 beyond).
+template <int MT, int MAXNT>
 __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_constant__ Args a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ int s_ids[kMaxT][kMaxK];
   __shared__ uint32_t s_tokmask[kMaxE];
   __shared__ int16_t s_d_of_e[kMaxE];
+  __shared__ int32_t s_slot[kMaxE];
   __shared__ int16_t s_act_e[kMaxE + 1];
   __shared__ int32_t s_act_slot[kMaxE + 1];
   __shared__ int16_t s_act_off[kMaxE + 1];
   __shared__ uint8_t s_act_cnt[kMaxE + 1];
-  __shared__ uint32_t s_warp[32];
+  __shared__ __align__(8) uint64_t s_bar[2 * kMaxNst + kPubBars];  // full, empty, publish
+  __shared__ int4 s_hdr[kMaxNst];                           // the job in each stage
   __shared__ uint32_t s_total;
   __shared__ int s_abort;
-  __shared__ int s_flag;
 
+  constexpr int UI = 32 * MT;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, bid = blockIdx.x;
   const int T = a.T, k = a.k, E = a.E, H = a.H;
@@ -404,19 +496,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
   const uint32_t sbase = smem_u32(smem);
-  float* const red = reinterpret_cast<float*>(smem + (size_t)kNst * a.stage_bytes);
-  const uint32_t full0 = sbase + kNst * a.stage_bytes + kRedBytes, empty0 = full0 + kNst * 8;
+  float* const red = reinterpret_cast<float*>(smem + (size_t)a.nst * a.stage_bytes);
+  uint8_t* const hbuf = smem + (size_t)a.nst * a.stage_bytes + red_bytes(MT);
+  const uint32_t full0 = smem_u32(&s_bar[0]), empty0 = full0 + 8 * kMaxNst,
+                 pub0 = empty0 + 8 * kMaxNst;
   volatile int* abort_flag = &s_abort;  // read in loops without barriers
 
-  for (int e = tid; e < E; e += kThreads) s_tokmask[e] = 0;
   if (tid == 0) {
     s_abort = 0;
-    for (int i = 0; i < kNst; ++i) {
+    for (int i = 0; i < a.nst; ++i) {
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, kCW);
     }
+    for (int i = 0; i < kPubBars; ++i) mbar_init(pub0 + 8 * i, kPubCount);
     fence_barrier_init();
+    // the tensor maps' descriptors (kernel parameters), fetched ahead of use
+    const CUtensorMap* maps[] = {&a.tm_gc, &a.tm_uc, &a.tm_dc, &a.tm_gs, &a.tm_us, &a.tm_ds, &a.tm_x};
+    for (const CUtensorMap* m : maps) prefetch_tensormap(m);
+    if (has_shared) {
+      const CUtensorMap* smaps[] = {&a.tm_sgc, &a.tm_suc, &a.tm_sdc, &a.tm_sgs, &a.tm_sus, &a.tm_sds};
+      for (const CUtensorMap* m : smaps) prefetch_tensormap(m);
+    }
+    // the next kernel of the stream may be scheduled now: it takes an SM only
+    // when a CTA of this one exits, and waits for this grid before reading
+    griddep_launch_dependents();
   }
+  for (int e = tid; e < E; e += kThreads) s_tokmask[e] = 0;
+  // nothing above reads global memory: from here on the previous kernel of the
+  // stream (which may have written the inputs or this workspace) is complete
+  griddep_wait();
+  // the slot map comes in by asynchronous copies while the routing runs
+  for (int e = tid; e < E; e += kThreads) {
+    if (a.slot_map) cp_async_4(&s_slot[e], a.slot_map + e);
+    else s_slot[e] = e;
+  }
+  cp_async_commit();
+  int ticket = 0;  // the producer's first unit (the atomic's latency overlaps the routing)
+  if (tid == 0) ticket = atomicAdd(a.sync + kSyncQueue, 1);
 
   // ---- routing: ids of every row (all CTAs); weights of row bid (CTA bid < T).
   // The stage buffers are still idle: they hold the top-k scratch.
@@ -441,9 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
           a.ids_out[(size_t)t * k + lane] = s_ids[t][lane];
           a.w_out[(size_t)t * k + lane] = (float)(ej / sum);
         }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) atomicAdd(a.sync + kSyncWReady, 1);
+        // published by this CTA's producer (a gpu-scope fence is slow and the
+        // combine that reads the weights comes much later)
       }
       __syncwarp();
     }
@@ -457,7 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
       s_ids[i / k][i % k] = e;
     }
   }
-  __syncthreads();  // the top-k scratch (stage memory) is released
+  cp_async_wait_all();
+  __syncthreads();  // the top-k scratch (stage memory) is released; the slot map is in
   // ---- permutation: token masks (shared atomics), then one warp builds the
   // active-expert list (ascending id), the offsets and the miss list
   for (int p = tid; p < T * k; p += kThreads) atomicOr(&s_tokmask[s_ids[p / k][p % k]], 1u << (p / k));
@@ -469,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     for (int e = e0; e < e1; ++e) {
       const uint32_t m = s_tokmask[e];
       if (!m) continue;
-      int slot = a.slot_map ? a.slot_map[e] : e;
+      int slot = s_slot[e];
       if (slot >= a.S) slot = -1;
       pack += slot >= 0 ? 1u + ((uint32_t)__popc(m) << 22) : (1u << 11);
     }
@@ -486,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
       int16_t dd = -1;
       const uint32_t m = s_tokmask[e];
       if (m) {
-        int slot = a.slot_map ? a.slot_map[e] : e;
+        int slot = s_slot[e];
         if (slot >= a.S) {
           if (bid == 0) atomicOr(a.status, DEV_BAD_SLOT);
           slot = -1;
@@ -519,246 +635,256 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     }
   }
   __syncthreads();
-  const uint32_t tot = s_total;
-  const int D = tot & 0x7ff, Pres = (tot >> 22) & 0x3ff;
-  const int nDx = D + (has_shared ? 1 : 0);
-  if (nDx == 0) {  // nothing resident and no shared expert: y = 0
-    const int n = T * H;
-    for (int i = bid * kThreads + tid; i < n; i += G * kThreads) a.y[i] = 0.f;
-  }
   __syncthreads();
-
-  // ---- work: gate/up units round-robin, then down units contiguous per CTA
-  Plan pl;
-  pl.nIu = a.I / kGuRows;
-  pl.D = D;
-  pl.nRg = H / a.R;
-  pl.nKc = H / a.KC;
-  pl.nKd = a.I / a.KCd;  // the shared expert's down has the same number of chunks
-  const int nIs = a.shI / kGuRows;
-  const int U1 = D * pl.nIu + (has_shared ? nIs : 0);
-  pl.nGu = bid < U1 ? (U1 - bid + G - 1) / G : 0;
-  const int U2 = nDx * pl.nRg;
-  pl.v0 = (int)((long long)bid * U2 / G);
-  pl.v1 = (int)((long long)(bid + 1) * U2 / G);
-  const int njobs = pl.njobs();
+  const uint32_t tot = s_total;
+  Sched sc;
+  sc.D = tot & 0x7ff;
+  const int Pres = (tot >> 22) & 0x3ff;
+  sc.nGs = has_shared ? a.shI / UI : 0;
+  sc.nGi = a.I / UI;
+  sc.total = sc.nGs + sc.D * sc.nGi;
+  const int D = sc.D;
+  const int nch = H / kKC;        // gate/up jobs (256 columns) per unit
+  const int nchd = H / kDnRows;   // down jobs (512 rows) per unit
+  // published units and routing-weight rows the reduction waits for
+  const int target = sc.total + (layer_mode ? T : 0);
 
   if (warp == 0) {
-    // ================= producer (lane 0 issues; the warp stays converged) =================
-    fence_proxy_async_shared();  // the top-k scratch in stage memory precedes the TMA writes
-    int issued = 0;
-    for (int j = 0; j < njobs; ++j) {
-      if (*abort_flag) break;
-      const Job jb = decode_job(j, pl, bid, G);
-      const int slot = j % kNst;
-      if (!mbar_wait_bounded(empty0 + 8 * slot, ((j / kNst) & 1) ^ 1, a.status)) {
-        *abort_flag = 1;
-        break;
-      }
-      const bool sh = jb.d == D;
-      const int slotp = sh ? 0 : s_act_slot[jb.d];
-      const uint32_t st = sbase + slot * a.stage_bytes;
-      const uint32_t fb = full0 + 8 * slot;
-      bool okh = true;
-      if (lane == 0) {
-        if (jb.gu) {
-          const int KC = a.KC, nl = KC / 256;
-          mbar_expect_tx(fb, (uint32_t)gu_bytes(KC, a.TB));
-          const int row = (sh ? 0 : slotp * a.I) + jb.tile * kGuRows;
-          const CUtensorMap* tq[2] = {sh ? &a.tm_sgc : &a.tm_gc, sh ? &a.tm_suc : &a.tm_uc};
-          const CUtensorMap* ts[2] = {sh ? &a.tm_sgs : &a.tm_gs, sh ? &a.tm_sus : &a.tm_us};
-          for (int mat = 0; mat < 2; ++mat) {
-            for (int L = 0; L < nl; ++L)
-              tma_load_2d(st + (mat * nl + L) * (kGuRows * 128), tq[mat],
-                          jb.kc * (KC / 2) + L * 128, row, fb);
-            tma_load_2d(st + gu_scales(KC, a.TB) + mat * kGuRows * (KC / 16), ts[mat], jb.kc * (KC / 32),
-                        row, fb);
+    if (lane == 0) {
+      // ================= producer (one thread) =================
+      fence_proxy_async_shared();  // the top-k scratch in stage memory precedes the TMA writes
+      Producer<MT> P{a, sbase, full0, empty0, pub0, s_hdr, s_act_slot, D,
+                     l2_evict_first_policy(), 0, 0, 0};
+      bool ok = true;
+      bool w_pub = !(layer_mode && bid < T);
+      int next = ticket;
+      while (ok && !*abort_flag && ticket < sc.total) {
+        if (P.ui - P.pd >= kUnitRing) {  // bound the unpublished units
+          const long long t0 = cycles_now();
+          while (ok && P.ui - P.pd >= kUnitRing) {
+            P.wait_pub(1000);
+            P.poll();
+            if (P.timed_out(t0)) ok = false;
           }
-          tma_load_3d(st + gu_x(KC), &a.tm_x, 0, jb.kc * (KC / 64), 0, fb);
-        } else {
-          const int KCd = sh ? a.KCds : a.KCd, nl = KCd / 256;
-          mbar_expect_tx(fb, (uint32_t)dn_bytes(a.R, KCd, a.TB));
-          const int row = (sh ? 0 : slotp * H) + jb.tile * a.R;
-          const CUtensorMap* tq = sh ? &a.tm_sdc : &a.tm_dc;
-          for (int L = 0; L < nl; ++L)
-            tma_load_2d(st + L * (a.R * 128), tq, jb.kc * (KCd / 2) + L * 128, row, fb);
-          tma_load_2d(st + dn_scales(a.R, KCd, a.TB), sh ? &a.tm_sds : &a.tm_ds, jb.kc * (KCd / 32), row,
-                      fb);
-          // the expert's h rows: only once all its gate/up units are done
-          okh = wait_counter_bounded(a.sync + kSyncReady + jb.d, sh ? nIs : pl.nIu, a.status);
-          if (okh) {
-            fence_proxy_async_global();
-            tma_load_3d(st + dn_h(a.R, KCd), sh ? &a.tm_hs : &a.tm_h, 0, jb.kc * (KCd / 64),
-                        s_act_off[jb.d], fb);
-          }
+          if (!ok) break;
+        }
+        const int2 u = sc.unit(ticket);
+        ++P.ui;
+        next = atomicAdd(a.sync + kSyncQueue, 1);  // needed at the next unit only
+        for (int ch = 0; ch < nch && ok; ++ch) ok = P.issue(J_GU, u.x, u.y, ch);
+        for (int ch = 0; ch < nchd && ok; ++ch) ok = P.issue(J_DN, u.x, u.y, ch);
+        ticket = next;
+        if (!w_pub) {  // row bid's routing weights, written before the permutation
+          w_pub = true;
+          __threadfence();
+          atomicAdd(a.sync + kSyncUnits, 1);
         }
       }
-      issued = j + 1;
-      if (!__shfl_sync(0xffffffffu, okh ? 1 : 0, 0)) {
-        *abort_flag = 1;
-        break;
+      if (ok) ok = P.issue(J_END, 0, 0, 0);
+      if (!w_pub) {
+        w_pub = true;
+        __threadfence();
+        atomicAdd(a.sync + kSyncUnits, 1);
       }
+      // every unit published
+      if (ok) {
+        const long long t0 = cycles_now();
+        for (uint32_t it = 1; ok && P.pd < P.ui; ++it) {
+          P.wait_pub(1000);
+          P.poll();
+          if ((it & 15) == 0 && P.pd < P.ui && P.timed_out(t0)) ok = false;
+        }
+      }
+      if (!ok) *abort_flag = 1;
+      // no copy may still be in flight when the CTA exits (bounded)
+      for (int jj = P.j - 1; jj >= 0 && jj >= P.j - a.nst; --jj)
+        mbar_wait_bounded(full0 + 8 * (jj % a.nst), (jj / a.nst) & 1, a.status);
     }
-    // no copy may still be in flight when the CTA exits (bounded)
-    if (lane == 0)
-      for (int j = issued - 1; j >= 0 && j >= issued - kNst; --j)
-        mbar_wait_bounded(full0 + 8 * (j % kNst), (j / kNst) & 1, a.status);
+    __syncwarp();
   } else {
     // ================= consumers =================
-    const int cw = warp - 1, ct = tid - 32;
+    const int cw = warp - 1, mw = cw & 3, kh = cw >> 2, ct = tid - 32;
     const int g = lane >> 2, c = lane & 3;
-    float acc[kMaxMT][2][4];
-    int brow[2] = {0, 0};  // row of token slot nt*8 + g in the x box (token) / h box (slot)
-    int cnt = 0, ntiles = 1;
-    for (int j = 0; j < njobs; ++j) {
-      const Job jb = decode_job(j, pl, bid, G);
-      const int slot = j % kNst;
-      const bool sh = jb.d == D;
-      if (jb.first) {
-#pragma unroll
-        for (int m = 0; m < kMaxMT; ++m)
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[m][nt][i] = 0.f;
-        cnt = s_act_cnt[jb.d];
-        ntiles = cnt > 8 ? 2 : 1;
-        const uint32_t mask = sh ? 0u : s_tokmask[s_act_e[jb.d]];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int nb = min(nt * 8 + g, cnt - 1);
-          brow[nt] = (jb.gu && !sh) ? nth_bit(mask, nb) : nb;
-        }
+    float* const rw = red + mw * (MT * 2 * 4 * 32);  // this row warp's exchange area
+    constexpr int HB = UI * 2 + 16;
+    float acc[MT][2][4];
+    float accd[kDnM][2][4];
+    int browx[2] = {0, 0};  // x box row (token) of token slot nt*8 + g
+    int browh[2] = {0, 0};  // h buffer row (slot) of token slot nt*8 + g
+    int cnt = 0, ntiles = 1, ucnt = 0;
+    for (int j = 0;; ++j) {
+      if (*abort_flag) break;
+      const int slot = j % a.nst;
+      if (!mbar_wait_bounded(full0 + 8 * slot, (j / a.nst) & 1, a.status)) {
+        *abort_flag = 1;
+        break;
       }
-      const bool ok = !*abort_flag && mbar_wait_bounded(full0 + 8 * slot, (j / kNst) & 1, a.status);
-      if (!ok) *abort_flag = 1;
-      const uint8_t* st = smem + (size_t)slot * a.stage_bytes;
-      const int MT = jb.gu ? 4 : a.R / 16;
-      if (ok) {
-        const int kcols = jb.gu ? a.KC : (sh ? a.KCds : a.KCd);
-        const int TB = a.TB;
-        if (jb.gu) {
-          if (ntiles == 1) job_compute<true, 4, 1>(st, kcols, a.R, TB, cw, brow, acc);
-          else job_compute<true, 4, 2>(st, kcols, a.R, TB, cw, brow, acc);
-        } else {
-          if (ntiles == 1) job_compute<false, 4, 1>(st, kcols, a.R, TB, cw, brow, acc);
-          else job_compute<false, 4, 2>(st, kcols, a.R, TB, cw, brow, acc);
+      const int4 hd = s_hdr[slot];
+      if (hd.x == J_END) break;
+      const int kind = hd.x, d = hd.y, grp = hd.z, chunk = hd.w;
+      const uint32_t st = sbase + slot * a.stage_bytes;
+      uint8_t* hb = hbuf + (ucnt & 1) * (kMaxT * HB);
+      const uint32_t hbs = smem_u32(hb);
+      if (kind == J_GU) {
+        if (chunk == 0) {
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) acc[m][nt][q] = 0.f;
+          const bool sh = d == D;
+          cnt = s_act_cnt[d];
+          ntiles = cnt > 8 ? 2 : 1;
+          const uint32_t mask = sh ? 0u : s_tokmask[s_act_e[d]];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const int nb = min(nt * 8 + g, cnt - 1);
+            browh[nt] = nb;
+            browx[nt] = sh ? nb : nth_bit(mask, nb);
+          }
         }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * slot);  // this warp is done with the stage
-      if (!jb.last) continue;
+        if (MAXNT == 1 || ntiles == 1) job_compute<true, MT, 1>(st, mw, kh, a.TB, browx, acc);
+        else job_compute<true, MT, MAXNT>(st, mw, kh, a.TB, browx, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * slot);  // this warp is done with the stage
+        if (chunk != nch - 1) continue;
 
-      // ---- unit epilogue: cross-warp reduction in fixed warp order
+        // ---- gate/up epilogue: half 1 hands its sums to half 0 (fixed order
+        // h0 + h1); h = silu(g) u goes to the unit's shared-memory h buffer
+        if (kh == 1) {
 #pragma unroll
-      for (int m = 0; m < kMaxMT; ++m)
+          for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+              if (nt < ntiles)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) rw[((m * 2 + nt) * 4 + q) * 32 + lane] = acc[m][nt][q];
+        }
+        named_bar_sync(1 + mw, 64);
+        if (kh == 0) {
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              if (nt >= ntiles) continue;
+              float v[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) v[q] = acc[m][nt][q] + rw[((m * 2 + nt) * 4 + q) * 32 + lane];
+              // v = (g, g, u, u) of unit row il for token slots 2c, 2c+1
+              const int il = 8 * (mw * MT + m) + g;
+              const int col = (il & ~7) + perm8_pos(il & 7);
+#pragma unroll
+              for (int e2 = 0; e2 < 2; ++e2) {
+                const int n = nt * 8 + 2 * c + e2;
+                const float gv = v[e2];
+                const float hv = gv / (1.0f + expf(-gv)) * v[2 + e2];
+                if (n < cnt && !(fabsf(hv) < 65504.f)) atomicOr(a.status, DEV_RANGE);
+                *reinterpret_cast<__half*>(hb + n * HB + 2 * col) = __float2half_rn(hv);
+              }
+            }
+        }
+        named_bar_sync(5, kCW * 32);  // h is complete; the exchange area is free again
+        continue;
+      }
+
+      // ---- down job: 256 output rows of this unit's slice of I
+#pragma unroll
+      for (int m = 0; m < kDnM; ++m)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
-          if (m < MT && nt < ntiles) {
-            float* slab = red + ((cw * kMaxMT + m) * 2 + nt) * kRed;
-            slab[(2 * c) * 17 + g] = acc[m][nt][0];
-            slab[(2 * c + 1) * 17 + g] = acc[m][nt][1];
-            slab[(2 * c) * 17 + g + 8] = acc[m][nt][2];
-            slab[(2 * c + 1) * 17 + g + 8] = acc[m][nt][3];
-          }
-      named_bar_sync(1, kCW * 32);
-      const bool good = !*abort_flag;
-      const int nl = ct >> 5, rl = ct & 31;
-      const int base = s_act_off[jb.d];
-      if (jb.gu) {
-        float hv[2];
-        const int mg = rl >> 4, rr = rl & 15;
-        for (int nt = 0; nt < ntiles; ++nt) {
-          float gs = 0.f, us = 0.f;
 #pragma unroll
-          for (int w = 0; w < kCW; ++w) {
-            gs += red[((w * kMaxMT + mg) * 2 + nt) * kRed + nl * 17 + rr];
-            us += red[((w * kMaxMT + 2 + mg) * 2 + nt) * kRed + nl * 17 + rr];
-          }
-          hv[nt] = gs / (1.0f + expf(-gs)) * us;
-        }
-        named_bar_sync(1, kCW * 32);  // red is read: the next unit may write it
-        for (int nt = 0; nt < ntiles; ++nt) {
-          const int n = nt * 8 + nl;
-          if (good && n < cnt) {
-            if (!(fabsf(hv[nt]) < 65504.f)) atomicOr(a.status, DEV_RANGE);
-            const int col = jb.tile * kGuRows + rl;
-            a.h[(size_t)(base + n) * a.Imax + (col & ~7) + perm8_pos(col & 7)] =
-                __half_as_ushort(__float2half_rn(hv[nt]));
-          }
-        }
-        named_bar_sync(1, kCW * 32);  // every h store of the unit is done (CTA scope)
-        if (ct == 0) red_release_gpu_add(a.sync + kSyncReady + jb.d, 1);  // publish + count
-      } else {
-        float ov[2][2];
-        for (int nt = 0; nt < ntiles; ++nt)
+          for (int q = 0; q < 4; ++q) accd[m][nt][q] = 0.f;
+      const int boff = (grp * MT) & 7;
+      if (MAXNT == 1 || ntiles == 1) dn_compute<MT, 1>(st, hbs, cw, boff, browh, accd);
+      else dn_compute<MT, MAXNT>(st, hbs, cw, boff, browh, accd);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+      {
+        const bool good = !*abort_flag;
+        const int base = s_act_off[d];
+        const int Gm = a.Gmax;
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int r = rl + 32 * q;
-            float o = 0.f;
-            if (r < a.R) {
-              const int m = r >> 4, rr = r & 15;
+        for (int m = 0; m < kDnM; ++m)
 #pragma unroll
-              for (int w = 0; w < kCW; ++w) o += red[((w * kMaxMT + m) * 2 + nt) * kRed + nl * 17 + rr];
-            }
-            ov[nt][q] = o;
-          }
-        named_bar_sync(1, kCW * 32);  // red is read: the next unit may write it
-        for (int nt = 0; nt < ntiles; ++nt) {
-          const int n = nt * 8 + nl;
+          for (int nt = 0; nt < 2; ++nt) {
+            if (nt >= ntiles) continue;
+            const int r = chunk * kDnRows + 16 * (kDnM * cw + m) + g;
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int r = rl + 32 * q;
-            if (good && n < cnt && r < a.R)
-              a.partial[(size_t)(base + n) * H + (size_t)jb.tile * a.R + r] = ov[nt][q];
-          }
-        }
-        named_bar_sync(1, kCW * 32);  // every partial store of the unit is done (CTA scope)
-        if (ct == 0) {
-          __threadfence();
-          const bool last = atomicAdd(a.sync + kSyncRg + jb.tile, 1) == nDx - 1;
-          if (last) __threadfence();  // acquire the other CTAs' partials
-          s_flag = last;
-        }
-        named_bar_sync(1, kCW * 32);
-        if (s_flag && good) {
-          // last contribution to this row group: y = sum_j w_j o_j (j order) + shared
-          bool wok = true;
-          if (layer_mode) wok = wait_counter_bounded(a.sync + kSyncWReady, T, a.status);
-          if (wok) {
-            for (int idx = ct; idx < T * a.R; idx += kCW * 32) {
-              const int t = idx / a.R, r = idx - t * a.R;
-              const size_t col = (size_t)jb.tile * a.R + r;
-              const float sv = has_shared ? ldg_cg_f32(a.partial + (size_t)(Pres + t) * H + col) : 0.f;
-              float yv = 0.f;
-              for (int j0 = 0; j0 < k; j0 += 8) {  // 8 pairs' loads in flight, summed in j order
-                float pv[8], wv[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  pv[q] = 0.f;
-                  wv[q] = 0.f;
-                  const int jj = j0 + q;
-                  if (jj < k) {
-                    const int e = s_ids[t][jj];
-                    const int dd = s_d_of_e[e];
-                    if (dd >= 0) {
-                      const int pos = s_act_off[dd] + __popc(s_tokmask[e] & ((1u << t) - 1u));
-                      wv[q] = layer_mode ? ldg_cg_f32(a.w_out + (size_t)t * k + jj)
-                                         : a.w_in[(size_t)t * k + jj];
-                      pv[q] = ldg_cg_f32(a.partial + (size_t)pos * H + col);
-                    }
-                  }
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                  if (j0 + q < k) yv = fmaf(wv[q], pv[q], yv);
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const int n = nt * 8 + 2 * c + e2;
+              if (good && n < cnt) {
+                float* pp = a.partial + ((size_t)(base + n) * Gm + grp) * H + r;
+                pp[0] = accd[m][nt][e2];
+                pp[8] = accd[m][nt][2 + e2];
               }
-              a.y[(size_t)t * H + col] = yv + sv;
             }
-          } else {
-            *abort_flag = 1;
           }
-          if (ct == 0) a.sync[kSyncRg + jb.tile] = 0;
+      }
+      if (chunk == nchd - 1) {
+        mbar_arrive(pub0 + 8 * (ucnt % kPubBars));  // every lane: its partial stores are done
+        ++ucnt;
+      }
+    }
+
+    // ---- reduction, once every unit of the window is published. Lane q of an
+    // 8-lane group sums, for one output float4,
+    //   v_q = sum_{j = q, q+8, ..} w_tj sum_g p(e_tj, g)[t] + sum_{g = q, q+8, ..} p(shared, g)[t]
+    // (g in order), and y = v_0 + ... + v_7 in lane order: a fixed order on every CTA.
+    if (!*abort_flag) {
+      if (ct == 0 && !wait_counter_bounded(a.sync + kSyncUnits, target, a.status)) *abort_flag = 1;
+      named_bar_sync(6, kCW * 32);
+      if (!*abort_flag) {
+        const int q = ct & 7, H4 = H / 4, NO = T * H4;
+        const size_t gstride = (size_t)a.Gmax * H;
+        for (int o0 = bid * (kCW * 4); o0 < NO; o0 += G * (kCW * 4)) {
+          const int o = o0 + (ct >> 3);
+          const bool live = o < NO;
+          const int t = live ? o / H4 : 0, col = live ? (o - t * H4) * 4 : 0;
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (live) {
+            for (int jj = q; jj < k; jj += 8) {
+              const int e = s_ids[t][jj];
+              const int dd = s_d_of_e[e];
+              if (dd < 0) continue;
+              const int pos = s_act_off[dd] + __popc(s_tokmask[e] & ((1u << t) - 1u));
+              const float wv = layer_mode ? ldg_cg_f32(a.w_out + (size_t)t * k + jj) : a.w_in[(size_t)t * k + jj];
+              const float* pp = a.partial + (size_t)pos * gstride + col;
+              float4 sacc = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int g0 = 0; g0 < sc.nGi; g0 += 8) {  // 8 slices' loads in flight
+                float4 pv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                  pv[u] = g0 + u < sc.nGi ? ldg_cg_f4(pp + (size_t)(g0 + u) * H) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  sacc.x += pv[u].x; sacc.y += pv[u].y; sacc.z += pv[u].z; sacc.w += pv[u].w;
+                }
+              }
+              v.x = fmaf(wv, sacc.x, v.x); v.y = fmaf(wv, sacc.y, v.y);
+              v.z = fmaf(wv, sacc.z, v.z); v.w = fmaf(wv, sacc.w, v.w);
+            }
+            if (has_shared) {
+              const float* pp = a.partial + (size_t)(Pres + t) * gstride + col;
+              for (int gg = q; gg < sc.nGs; gg += 8) {
+                const float4 u4 = ldg_cg_f4(pp + (size_t)gg * H);
+                v.x += u4.x; v.y += u4.y; v.z += u4.z; v.w += u4.w;
+              }
+            }
+          }
+          // lanes q = 0..7 of the group, summed in lane order
+          float4 y4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int s2 = 0; s2 < 8; ++s2) {
+            y4.x += __shfl_sync(0xffffffffu, v.x, (lane & ~7) + s2);
+            y4.y += __shfl_sync(0xffffffffu, v.y, (lane & ~7) + s2);
+            y4.z += __shfl_sync(0xffffffffu, v.z, (lane & ~7) + s2);
+            y4.w += __shfl_sync(0xffffffffu, v.w, (lane & ~7) + s2);
+          }
+          if (live && q == 0) {
+            float* yp = a.y + (size_t)t * H + col;
+            yp[0] = y4.x; yp[1] = y4.y; yp[2] = y4.z; yp[3] = y4.w;
+          }
         }
       }
     }
@@ -769,9 +895,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(a.sync + kSyncDone, 1) == G - 1) {
-      for (int d = 0; d <= D; ++d) a.sync[kSyncReady + d] = 0;
-      for (int rg = 0; rg < pl.nRg; ++rg) a.sync[kSyncRg + rg] = 0;
-      a.sync[kSyncWReady] = 0;
+      a.sync[kSyncUnits] = 0;
+      a.sync[kSyncQueue] = 0;
       a.sync[kSyncDone] = 0;
       __threadfence();
     }
@@ -793,68 +918,6 @@ static int num_sms() {
 }
 
 namespace {
-struct FusedCfg {
-  int KC, KCd, KCds, R, stage_bytes;
-};
-
-constexpr int kStageCap = 48 * 1024;
-
-// Largest chunk c of K (a multiple of 256 dividing K, at most cap).
-int chunk_of(int K, int cap) {
-  for (int c = cap; c >= 256; c -= 256)
-    if (K % c == 0) return c;
-  return 0;
-}
-
-// The chunking: gate/up chunks of H, down rows per unit and down chunks of I
-// such that one job (weights + TB activation rows) fits a stage. Warps take
-// blocks b = w (mod 8) whatever the chunk size, and the down rows R do not
-// depend on TB, so a row's arithmetic is the same in any window.
-bool fused_cfg(int H, int I, int shI, int TB, FusedCfg* out) {
-  FusedCfg f{};
-  f.KC = chunk_of(H, 512);
-  if (!f.KC) return false;
-  int sb = fused::gu_bytes(f.KC, TB);
-  f.R = 0;
-  int Rfix = 0;  // the rows per down unit, fixed by the largest window
-  for (int R = 64; R >= 64 && !Rfix; R /= 2) {  // the kernel handles 64-row down units only
-    if (H % R) continue;
-    for (int c = 256; c <= I; c += 256)
-      if (I % c == 0 && fused::dn_bytes(R, c, fused::kMaxT) <= kStageCap) {
-        Rfix = R;
-        break;
-      }
-  }
-  for (int R = Rfix; R == Rfix && R >= 16 && !f.R; R = 0) {
-    for (int cap = 2048; cap >= 256; cap -= 256) {
-      const int c = chunk_of(I, cap);
-      if (!c) continue;
-      const int nk = I / c;
-      int bytes = fused::dn_bytes(R, c, TB);
-      int cs = 0;
-      if (shI > 0) {
-        if (shI % nk) continue;
-        cs = shI / nk;
-        if (cs % 256) continue;
-        const int bs = fused::dn_bytes(R, cs, TB);
-        bytes = bytes > bs ? bytes : bs;
-      }
-      if (bytes <= kStageCap) {
-        f.R = R;
-        f.KCd = c;
-        f.KCds = cs ? cs : c;
-        sb = sb > bytes ? sb : bytes;
-        break;
-      }
-    }
-  }
-  if (!f.R) return false;
-  f.stage_bytes = (sb + 1023) & ~1023;
-  if (fused::smem_bytes(f.stage_bytes) + 20 * 1024 > 227 * 1024) return false;
-  *out = f;
-  return true;
-}
-
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
 // dependency on libcuda).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -889,8 +952,9 @@ struct MapKeyHash {
 };
 
 // Encode (or fetch from a small cache) a 2D or 3D tiled tensor map.
+// swz_bytes: the swizzle span (128, 64 or 32 bytes), anything else for none.
 bool tensor_map(CUtensorMap* out, CUtensorMapDataType dt, const void* ptr, int rank,
-                const uint64_t* dims, const uint64_t* strides, const uint32_t* box, bool swizzle) {
+                const uint64_t* dims, const uint64_t* strides, const uint32_t* box, int swz_bytes) {
   static std::mutex mu;
   static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
   MapKey key;
@@ -900,7 +964,7 @@ bool tensor_map(CUtensorMap* out, CUtensorMapDataType dt, const void* ptr, int r
   key.s1 = strides[0]; key.s2 = rank > 2 ? strides[1] : 0;
   key.b0 = box[0]; key.b1 = box[1]; key.b2 = rank > 2 ? box[2] : 0;
   key.dtype = (uint32_t)dt;
-  key.swz = swizzle ? 1 : 0;
+  key.swz = (uint32_t)swz_bytes;
   std::lock_guard<std::mutex> lk(mu);
   auto it = cache.find(key);
   if (it != cache.end()) {
@@ -913,7 +977,10 @@ bool tensor_map(CUtensorMap* out, CUtensorMapDataType dt, const void* ptr, int r
   CUtensorMap m;
   CUresult r = fn(&m, dt, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  swz_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                  : swz_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                  : swz_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                    : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   if (cache.size() > 4096) cache.clear();
@@ -922,87 +989,117 @@ bool tensor_map(CUtensorMap* out, CUtensorMapDataType dt, const void* ptr, int r
   return true;
 }
 
-// Codes [rows][K/2] bytes: box 128 bytes x box_rows, 128-byte swizzle.
-bool codes_map(CUtensorMap* m, const uint8_t* q, int K, int rows, int box_rows) {
+// Codes [rows][K/2] bytes: box box_bytes x box_rows, swizzled by the box's row
+// width (128, 64 or 32 bytes; 16-byte rows need none).
+bool codes_map(CUtensorMap* m, const uint8_t* q, int K, int rows, int box_bytes, int box_rows) {
   const uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)rows};
   const uint64_t str[1] = {(uint64_t)K / 2};
-  const uint32_t box[2] = {128, (uint32_t)box_rows};
-  return tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, 2, dims, str, box, true);
+  const uint32_t box[2] = {(uint32_t)box_bytes, (uint32_t)box_rows};
+  return tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, 2, dims, str, box, box_bytes);
 }
-// Scales [rows][K/32] fp16: box (chunk/32) x box_rows, no swizzle.
-bool scales_map(CUtensorMap* m, const uint16_t* s, int K, int rows, int chunk, int box_rows) {
+// Scales [rows][K/32] fp16: box 8 (256 columns) x box_rows, no swizzle.
+bool scales_map(CUtensorMap* m, const uint16_t* s, int K, int rows, int box_rows) {
   const uint64_t dims[2] = {(uint64_t)K / 32, (uint64_t)rows};
   const uint64_t str[1] = {(uint64_t)K / 16};
-  const uint32_t box[2] = {(uint32_t)chunk / 32, (uint32_t)box_rows};
-  return tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, s, 2, dims, str, box, false);
+  const uint32_t box[2] = {8, (uint32_t)box_rows};
+  return tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, s, 2, dims, str, box, 16);
 }
-// 16-bit activations [rows][cols]: viewed as (64, cols/64, rows); box (64, chunk/64, box_rows).
-bool act_map(CUtensorMap* m, const void* p, int cols, int rows, int chunk, int box_rows) {
+// 16-bit activations [rows][cols]: viewed as (64, cols/64, rows); box (64, 4, box_rows).
+bool act_map(CUtensorMap* m, const void* p, int cols, int rows, int box_rows) {
   const uint64_t dims[3] = {64, (uint64_t)cols / 64, (uint64_t)rows};
   const uint64_t str[2] = {128, (uint64_t)cols * 2};
-  const uint32_t box[3] = {64, (uint32_t)chunk / 64, (uint32_t)box_rows};
-  return tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, p, 3, dims, str, box, true);
+  const uint32_t box[3] = {64, 4, (uint32_t)box_rows};
+  return tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, p, 3, dims, str, box, 128);
 }
 }  // namespace
 
+
 static int box_rows(int T) { return T <= 8 ? 8 : 16; }
+
+// Rows per unit: UI = 32 MT intermediate rows. The largest MT that still gives
+// every SM a unit, by the expected number of distinct experts of T rows routed
+// uniformly (skewed routing touches fewer). MT decides which rows a warp owns
+// and how I is cut into slices for the down partials.
+int fused_choose_mt(int E, int k, int T, int I, int shI) {
+  const double p = 1.0 - (double)k / (double)E;
+  double pt = 1.0;
+  for (int t = 0; t < T; ++t) pt *= p;
+  const double d_est = (double)E * (1.0 - pt);
+  const int G = num_sms();
+  for (int mt = 4; mt > 1; mt /= 2) {
+    const int ui = 32 * mt;
+    if (I % ui || (shI % ui)) continue;
+    const double units = d_est * (I / ui) + shI / ui;
+    if (units >= G) return mt;
+  }
+  return 1;
+}
+
+int fused_partial_slices(int E, int k, int T, int I, int shI) {
+  const int mt = fused_choose_mt(E, k, T, I, shI);
+  return (I > shI ? I : shI) / (32 * mt);
+}
+
+template <int MT, int NTX>
+static cudaError_t kernel_attrs(size_t* static_smem, int* optin) {
+  static std::mutex mu;
+  static size_t st = 0;
+  static int opt = 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (opt == 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fused::decode_layer_kernel<MT, NTX>);
+    if (e != cudaSuccess) return e;
+    int dev = 0, o = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&o, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    st = fa.sharedSizeBytes;
+    opt = o;
+  }
+  *static_smem = st;
+  *optin = opt;
+  return cudaSuccess;
+}
+
+// Stages that fit next to the kernel's static shared memory (0: not even two).
+template <int MT, int NTX>
+static int stages_for(int TB) {
+  size_t st = 0;
+  int optin = 0;
+  if (kernel_attrs<MT, NTX>(&st, &optin) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int stage = fused::stage_bytes_for(MT, TB);
+  int n = fused::kMaxNst;
+  while (n >= 2 && fused::smem_bytes(MT, n, stage) + st > (size_t)optin) --n;
+  return n >= 2 ? n : 0;
+}
 
 bool fused_decode_supported(int H, int I, int shI, int T, bool x_bf16) {
   if (!x_bf16 || T < 1 || T > fused::kMaxT) return false;
-  if (H % 256 || I % 256 || shI % 256) return false;
+  if (H % fused::kDnRows || I % 256 || shI % 256) return false;
   if (H > 8192 || T > num_sms()) return false;
   if (!encode_fn()) return false;
-  FusedCfg f;
-  return fused_cfg(H, I, shI, box_rows(T), &f);
+  const int TB = box_rows(T);
+  if (TB == 8)
+    return stages_for<4, 1>(TB) >= 2 && stages_for<2, 1>(TB) >= 2 && stages_for<1, 1>(TB) >= 2;
+  return stages_for<4, 2>(TB) >= 2 && stages_for<2, 2>(TB) >= 2 && stages_for<1, 2>(TB) >= 2;
 }
 
-cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st) {
-  FusedCfg cfg;
-  const int TB = box_rows(f.T);
-  if (!fused_cfg(f.H, f.I, f.shI, TB, &cfg)) return cudaErrorInvalidValue;
-  fused::Args a;
-  std::memset(&a, 0, sizeof a);
-  a.H = f.H; a.I = f.I; a.shI = f.shI; a.E = f.E; a.k = f.k; a.S = f.S; a.T = f.T;
-  a.Imax = f.Imax;
-  a.KC = cfg.KC;
-  a.KCd = cfg.KCd;
-  a.KCds = cfg.KCds;
-  a.R = cfg.R;
-  a.stage_bytes = cfg.stage_bytes;
-  a.TB = TB;
-  a.rows_cap = f.rows_cap;
-  const int H = f.H, I = f.I, S = f.S;
-  bool ok = codes_map(&a.tm_gc, f.gq, H, S * I, fused::kGuRows) &&
-            codes_map(&a.tm_uc, f.uq, H, S * I, fused::kGuRows) &&
-            codes_map(&a.tm_dc, f.dq, I, S * H, cfg.R) &&
-            scales_map(&a.tm_gs, f.gs, H, S * I, cfg.KC, fused::kGuRows) &&
-            scales_map(&a.tm_us, f.us, H, S * I, cfg.KC, fused::kGuRows) &&
-            scales_map(&a.tm_ds, f.ds, I, S * H, cfg.KCd, cfg.R) &&
-            act_map(&a.tm_x, f.x, H, f.T, cfg.KC, TB) &&
-            act_map(&a.tm_h, f.hhi, f.Imax, f.rows_cap, cfg.KCd, TB);
-  if (ok && f.shI > 0)
-    ok = codes_map(&a.tm_sgc, f.sgq, H, f.shI, fused::kGuRows) &&
-         codes_map(&a.tm_suc, f.suq, H, f.shI, fused::kGuRows) &&
-         codes_map(&a.tm_sdc, f.sdq, f.shI, H, cfg.R) &&
-         scales_map(&a.tm_sgs, f.sgs, H, f.shI, cfg.KC, fused::kGuRows) &&
-         scales_map(&a.tm_sus, f.sus, H, f.shI, cfg.KC, fused::kGuRows) &&
-         scales_map(&a.tm_sds, f.sds, f.shI, H, cfg.KCds, cfg.R) &&
-         act_map(&a.tm_hs, f.hhi, f.Imax, f.rows_cap, cfg.KCds, TB);
-  if (!ok) return cudaErrorInvalidValue;
-  a.logits = f.logits; a.ids_in = f.ids_in; a.w_in = f.w_in;
-  a.slot_map = f.slot_map;
-  a.ids_out = f.ids_out; a.w_out = f.w_out; a.y = f.y;
-  a.miss_ids = f.miss_ids; a.n_miss = f.n_miss;
-  a.h = f.hhi;
-  a.partial = f.partial;
-  a.status = f.status; a.sync = f.sync;
-  const size_t smem = fused::smem_bytes(a.stage_bytes);
+template <int MT, int NTX>
+static cudaError_t launch_mt(fused::Args& a, cudaStream_t st) {
+  a.stage_bytes = fused::stage_bytes_for(MT, a.TB);
+  a.nst = stages_for<MT, NTX>(a.TB);
+  if (a.nst < 2) return cudaErrorInvalidValue;
+  const size_t smem = fused::smem_bytes(MT, a.nst, a.stage_bytes);
   static std::mutex mu;
   static size_t configured = 0;
   {
     std::lock_guard<std::mutex> lk(mu);
     if (smem > configured) {
-      cudaError_t e = cudaFuncSetAttribute(fused::decode_layer_kernel,
+      cudaError_t e = cudaFuncSetAttribute(fused::decode_layer_kernel<MT, NTX>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) {
         cudaGetLastError();
@@ -1011,10 +1108,68 @@ cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st) {
       configured = smem;
     }
   }
+  // programmatic dependent launch: the kernel's set-up overlaps the end of the
+  // previous kernel in the stream (the kernel waits for it before reading)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms());
+  cfg.blockDim = dim3(fused::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   launch_begin(K_FUSED, st);
-  fused::decode_layer_kernel<<<num_sms(), fused::kThreads, smem, st>>>(a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, fused::decode_layer_kernel<MT, NTX>, a);
   launch_end(st);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st) {
+  const int TB = box_rows(f.T);
+  const int MT = fused_choose_mt(f.E, f.k, f.T, f.I, f.shI);
+  const int UI = 32 * MT, DR = 256;  // down boxes of 256 rows
+  fused::Args a;
+  std::memset(&a, 0, sizeof a);
+  a.H = f.H; a.I = f.I; a.shI = f.shI; a.E = f.E; a.k = f.k; a.S = f.S; a.T = f.T;
+  a.Gmax = (f.I > f.shI ? f.I : f.shI) / UI;
+  a.TB = TB;
+  a.rows_cap = f.rows_cap;
+  const int H = f.H, I = f.I, S = f.S;
+  bool ok = codes_map(&a.tm_gc, f.gq, H, S * I, 128, UI) &&
+            codes_map(&a.tm_uc, f.uq, H, S * I, 128, UI) &&
+            codes_map(&a.tm_dc, f.dq, I, S * H, UI / 2, DR) &&
+            scales_map(&a.tm_gs, f.gs, H, S * I, UI) &&
+            scales_map(&a.tm_us, f.us, H, S * I, UI) &&
+            scales_map(&a.tm_ds, f.ds, I, S * H, DR) &&
+            act_map(&a.tm_x, f.x, H, f.T, TB);
+  if (ok && f.shI > 0)
+    ok = codes_map(&a.tm_sgc, f.sgq, H, f.shI, 128, UI) &&
+         codes_map(&a.tm_suc, f.suq, H, f.shI, 128, UI) &&
+         codes_map(&a.tm_sdc, f.sdq, f.shI, H, UI / 2, DR) &&
+         scales_map(&a.tm_sgs, f.sgs, H, f.shI, UI) &&
+         scales_map(&a.tm_sus, f.sus, H, f.shI, UI) &&
+         scales_map(&a.tm_sds, f.sds, f.shI, H, DR);
+  if (!ok) return cudaErrorInvalidValue;
+  a.logits = f.logits; a.ids_in = f.ids_in; a.w_in = f.w_in;
+  a.slot_map = f.slot_map;
+  a.ids_out = f.ids_out; a.w_out = f.w_out; a.y = f.y;
+  a.miss_ids = f.miss_ids; a.n_miss = f.n_miss;
+  a.partial = f.partial;
+  a.status = f.status; a.sync = f.sync;
+  if (TB == 8) {
+    switch (MT) {
+      case 4: return launch_mt<4, 1>(a, st);
+      case 2: return launch_mt<2, 1>(a, st);
+      default: return launch_mt<1, 1>(a, st);
+    }
+  }
+  switch (MT) {
+    case 4: return launch_mt<4, 2>(a, st);
+    case 2: return launch_mt<2, 2>(a, st);
+    default: return launch_mt<1, 2>(a, st);
+  }
 }
 
 }  // namespace moe

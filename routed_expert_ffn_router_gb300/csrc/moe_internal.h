@@ -101,6 +101,9 @@ struct FusedLaunch {
   int32_t* sync;
 };
 bool fused_decode_supported(int H, int I, int shI, int T, bool x_bf16);
+// Slices of I per partial row of the one-launch path (the partial buffer holds
+// rows x slices x H floats).
+int fused_partial_slices(int E, int k, int T, int I, int shI);
 cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st);
 
 }  // namespace moe
