@@ -399,6 +399,10 @@ static moe_status expert_ffn_impl(const moe_layer_desc* Ld, const void* x, moe_d
   a.partial = at<float>(ws, L.partial);
   a.y = y;
   a.status = o.status;
+  if (prefill_tc_supported(a.H, a.I, a.shI, T, x_dtype == MOE_BF16)) {
+    if ((e = launch_ffn_prefill_tc(a, x, st)) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(launch_combine(a, st));
+  }
   return cuda_status(launch_ffn_decode(a, x, x_dtype == MOE_BF16, L.cu_max, st));
 }
 

@@ -474,4 +474,13 @@ cudaError_t launch_ffn_decode(const FfnArgs& a, const void* x, bool x_bf16, int 
   return cudaGetLastError();
 }
 
+// The ordered combine alone (the prefill path runs its own GEMM kernels first).
+cudaError_t launch_combine(const FfnArgs& a, cudaStream_t st) {
+  dim3 grid((a.H / 4 + 255) / 256, a.T);
+  launch_begin(K_COMBINE, st);
+  combine_kernel<<<grid, 256, 0, st>>>(a, a.shI > 0 ? 1 : 0);
+  launch_end(st);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

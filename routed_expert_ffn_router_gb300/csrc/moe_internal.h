@@ -75,6 +75,13 @@ cudaError_t launch_ffn_decode(const FfnArgs& a, const void* x, bool x_bf16, int 
                               cudaStream_t st);
 
 int cu_bound(int T, int E, int k, bool has_shared);
+cudaError_t launch_combine(const FfnArgs& a, cudaStream_t st);
+
+// The prefill path on the tcgen05 tensor cores (moe_prefill.cu): gate/up +
+// SwiGLU into expert-sorted h, down into weighted partials; launch_combine
+// then forms y.
+bool prefill_tc_supported(int H, int I, int shI, int T, bool x_bf16);
+cudaError_t launch_ffn_prefill_tc(const FfnArgs& a, const void* x, cudaStream_t st);
 
 // The one-launch decode path (moe_fused.cu).
 struct FusedLaunch {

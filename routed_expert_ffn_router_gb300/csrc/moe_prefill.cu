@@ -1,0 +1,581 @@
+// Prefill path (prompt chunks): the routed experts' gate/up + SwiGLU and down
+// as grouped GEMMs on the 5th-generation tensor cores (tcgen05, TMEM
+// accumulators), over int4 blocks dequantised in shared memory.
+//
+// The pages' prompt path is a batched quantised GEMM in which a token batch
+// shares one weight read, grouped by expert (SGLang port post, section 2, the
+// expert-scoped layout that computes only the rows routed to each expert, and
+// section 3, the MMQ-class kernel); the grouping here is the (token, expert)
+// permutation: an expert's tokens are consecutive rows of the sorted order.
+//
+// Two persistent kernels, one per GEMM, each a warp-specialised pipeline:
+//   warp 8 (one thread) streams a job's int4 codes and fp16 scales (TMA tensor
+//   copies, 256 columns of K per raw stage) and its B operand (64 columns of K
+//   per stage, one TMA box of its rows of the expert-sorted x or h);
+//   warps 4-7 dequantise a raw stage into fp16 A tiles (128 rows x 64, K-major,
+//   128-byte swizzle): q = (1024 + (q ^ 8)) - 1032 exactly, then q * s with the
+//   fp16 scale, rounded once (2^-12);
+//   warp 9 (one thread) issues tcgen05.mma (M = 128, N = the job's tokens
+//   rounded up to 16, K = 16 per instruction) into one of two TMEM buffers and
+//   commits each stage back to its producers;
+//   warps 0-3 (one TMEM lane quarter each) drain the accumulators: h =
+//   silu(g) u in fp16 (gate/up), or w * (W_d h) as fp32 partials (down).
+// Both operands are fp16: the tensor cores take one type for A and B, and fp16
+// keeps q * s and h to 2^-12 where bf16 would round to 2^-9. x enters as
+// x / 2^e_t in fp16, written once per routed pair in the expert-sorted row
+// order (x16_prep_kernel; e_t is the smallest power of two that keeps the row
+// below 2^15, 0 for ordinary activations): exact for every bf16 value in
+// range, and the gate/up epilogue multiplies g and u back by 2^e_t.
+// A job is (active expert, 128 weight rows, up to 128 of its tokens); CTA b
+// takes jobs b, b + G, ... of the list both kernels derive from the
+// permutation. The ordered combine (moe_decode.cu) then sums the partials in
+// j order and adds the shared expert, which enters as one more expert with all
+// T tokens.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace pf {
+
+constexpr int kBM = 128;              // weight rows per job (M of the MMA)
+constexpr int kNT = 128;              // tokens per job at most (N of the MMA)
+constexpr int kRawSt = 2, kASt = 2, kBSt = 4;
+constexpr int kThreads = 320;         // warps 0-3 epilogue, 4-7 dequant, 8 producer, 9 MMA
+constexpr int kMaxAct = kMaxE + 1;
+constexpr int kCodeBox = 128 * 128;   // one raw code box: 128 rows x 128 bytes (256 columns)
+constexpr int kScaleBox = 128 * 16;   // one raw scale box: 128 rows x 8 fp16
+constexpr int kATile = 128 * 128;     // one fp16 A tile: 128 rows x 64 columns
+constexpr int kBTile = kNT * 128;     // one fp16 B tile: up to 128 rows x 64 columns
+
+struct Args {
+  CUtensorMap tm_c[2], tm_s[2];       // routed codes / scales (gate, up; or down)
+  CUtensorMap tm_sc[2], tm_ss[2];     // the shared expert's
+  CUtensorMap tm_b;                   // expert-sorted x16 [rows][H] or h [rows][Imax], fp16
+  int H, I, shI, k, T, P, Imax;
+  const ActExpert* act;
+  const int32_t* counters;            // [0]: active experts including the shared one
+  const int32_t* sorted_pair;
+  const float* w;
+  const float* xscale;                // 2^e_t per token (gate/up)
+  uint16_t* h;                        // fp16 [rows][Imax], expert-sorted rows
+  float* partial;                     // [rows][H]
+  int32_t* status;
+};
+
+template <bool GU>
+__host__ __device__ constexpr int nmat() { return GU ? 2 : 1; }
+template <bool GU>
+__host__ __device__ constexpr int raw_bytes() { return nmat<GU>() * (kCodeBox + kScaleBox); }
+template <bool GU>
+__host__ __device__ constexpr size_t smem_bytes() {
+  return 1024 + (size_t)kRawSt * raw_bytes<GU>() + (size_t)kASt * nmat<GU>() * kATile +
+         (size_t)kBSt * kBTile;
+}
+
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  // K-major, 128-byte swizzle: start address, leading offset 16 B (unused),
+  // 1024 B between 8-row groups, descriptor version 1, layout SWIZZLE_128B
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// kind::f16 instruction descriptor: fp32 accumulator, fp16 A and B, both K-major.
+__device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tc_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void st_s128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+// One 32-bit word of codes (columns 8c..8c+7, nibble i = column 8c+i) -> four
+// f16x2 registers holding q * s for columns (0,1), (2,3), (4,5), (6,7).
+__device__ __forceinline__ void dequant_word_h(uint32_t wd, __half2 s2, uint32_t (&o)[4]) {
+  const uint32_t mask = 0x000F000Fu, magic = 0x64086408u;  // f16 1024 + (q ^ 8) = 1032 + q
+  const uint32_t x0 = lop3_and_xor(wd, mask, magic), x1 = lop3_and_xor(wd >> 4, mask, magic);
+  const uint32_t x2 = lop3_and_xor(wd >> 8, mask, magic), x3 = lop3_and_xor(wd >> 12, mask, magic);
+  const uint32_t p[4] = {prmt(x0, x1, 0x5410), prmt(x2, x3, 0x5410), prmt(x0, x1, 0x7632), prmt(x2, x3, 0x7632)};
+  const __half2 m1032 = __floats2half2_rn(1032.f, 1032.f);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 v = *reinterpret_cast<const __half2*>(&p[i]);
+    v = __hmul2(__hsub2(v, m1032), s2);  // q exactly, then one rounding of q * s
+    o[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+}
+
+struct Job {
+  int a, mt, n0, nn, np;   // active entry, row tile, first token slot, tokens, tokens rounded to 16
+  int off, slot;           // first sorted row of the expert; pool slot (-1: shared)
+  bool sh;
+};
+
+template <bool GU>
+__global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__ Args a) {
+  constexpr int NM = nmat<GU>();
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t s_bar[2 * kRawSt + 2 * kASt + 2 * kBSt + 4];
+  __shared__ int s_js[kMaxAct + 1];      // first job of each active entry
+  __shared__ int s_off[kMaxAct], s_cnt[kMaxAct], s_slot[kMaxAct];
+  __shared__ float s_colf[2][kNT];       // per token column: x prescale (gate/up) or routing weight (down)
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, bid = blockIdx.x;
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+  const uint32_t sraw = smem_u32(smem);
+  const uint32_t sA = sraw + kRawSt * raw_bytes<GU>();
+  const uint32_t sB = sA + kASt * NM * kATile;
+  const uint32_t bar0 = smem_u32(&s_bar[0]);
+  const uint32_t raw_full = bar0, raw_empty = raw_full + 8 * kRawSt;
+  const uint32_t a_full = raw_empty + 8 * kRawSt, a_empty = a_full + 8 * kASt;
+  const uint32_t b_full = a_empty + 8 * kASt, b_empty = b_full + 8 * kBSt;
+  const uint32_t acc_full = b_empty + 8 * kBSt, acc_empty = acc_full + 16;
+  volatile int* abort_flag = &s_abort;
+
+  if (tid == 0) {
+    s_abort = 0;
+    for (int i = 0; i < kRawSt; ++i) {
+      mbar_init(raw_full + 8 * i, 1);
+      mbar_init(raw_empty + 8 * i, 128);
+    }
+    for (int i = 0; i < kASt; ++i) {
+      mbar_init(a_full + 8 * i, 128);
+      mbar_init(a_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < kBSt; ++i) {
+      mbar_init(b_full + 8 * i, 1);
+      mbar_init(b_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(acc_full + 8 * i, 1);
+      mbar_init(acc_empty + 8 * i, 128);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 9) {  // the whole TMEM (512 columns): two accumulator buffers of 256
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&s_tmem)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  // the job list: per active entry, (rows / 128) row tiles x ceil(tokens / 128)
+  const int n_act = min(a.counters[0], kMaxAct);
+  const int P = a.P;
+  for (int i = tid; i < n_act; i += kThreads) {
+    const ActExpert e = a.act[i];
+    s_off[i] = e.off;
+    s_cnt[i] = e.cnt;
+    s_slot[i] = e.slot;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (n_act + 31) / 32, i0 = lane * per, i1 = min(n_act, i0 + per);
+    int sum = 0;
+    for (int i = i0; i < i1; ++i) {
+      const int rows = GU ? (s_slot[i] < 0 ? a.shI : a.I) : a.H;
+      sum += (rows / kBM) * ((s_cnt[i] + kNT - 1) / kNT);
+    }
+    int x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    int run = x - sum;
+    for (int i = i0; i < i1; ++i) {
+      s_js[i] = run;
+      const int rows = GU ? (s_slot[i] < 0 ? a.shI : a.I) : a.H;
+      run += (rows / kBM) * ((s_cnt[i] + kNT - 1) / kNT);
+    }
+    if (lane == 31) s_js[n_act] = x;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int njobs = s_js[n_act];
+
+  auto job_of = [&](int j) {
+    int lo = 0, hi = n_act - 1;  // last entry with s_js <= j
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_js[mid] <= j) lo = mid;
+      else hi = mid - 1;
+    }
+    Job jb;
+    jb.a = lo;
+    jb.sh = s_slot[lo] < 0;
+    const int rows = GU ? (jb.sh ? a.shI : a.I) : a.H;
+    const int nM = rows / kBM;
+    const int loc = j - s_js[lo];
+    jb.mt = loc % nM;
+    jb.n0 = (loc / nM) * kNT;
+    jb.nn = min(kNT, s_cnt[lo] - jb.n0);
+    jb.np = (jb.nn + 15) & ~15;
+    jb.off = s_off[lo];
+    jb.slot = s_slot[lo];
+    return jb;
+  };
+  auto k_of = [&](const Job& jb) { return GU ? a.H : (jb.sh ? a.shI : a.I); };
+
+  if (warp == 8) {
+    // ================= producer =================
+    int rcnt = 0, bcnt = 0;
+    const uint64_t wpol = l2_evict_first_policy();
+    for (int j = bid; j < njobs && !*abort_flag; j += G) {
+      const Job jb = job_of(j);
+      if (lane == 0) {
+        const int K = k_of(jb);
+        const int row0 = (jb.sh ? 0 : jb.slot * (GU ? a.I : a.H)) + jb.mt * kBM;
+        bool ok = true;
+        for (int kr = 0; kr < K / 256 && ok; ++kr) {
+          const int rs = rcnt % kRawSt;
+          if (!(ok = mbar_wait_bounded(raw_empty + 8 * rs, ((rcnt / kRawSt) & 1) ^ 1, a.status))) break;
+          const uint32_t st = sraw + rs * raw_bytes<GU>(), fb = raw_full + 8 * rs;
+          mbar_expect_tx(fb, raw_bytes<GU>());
+#pragma unroll
+          for (int m = 0; m < NM; ++m) {
+            tma_load_2d_hint(st + m * kCodeBox, jb.sh ? &a.tm_sc[m] : &a.tm_c[m], kr * 128, row0, fb, wpol);
+            tma_load_2d_hint(st + NM * kCodeBox + m * kScaleBox, jb.sh ? &a.tm_ss[m] : &a.tm_s[m], kr * 8,
+                             row0, fb, wpol);
+          }
+          ++rcnt;
+          for (int kb = 0; kb < 4 && ok; ++kb) {
+            const int bs = bcnt % kBSt;
+            if (!(ok = mbar_wait_bounded(b_empty + 8 * bs, ((bcnt / kBSt) & 1) ^ 1, a.status))) break;
+            const uint32_t dst = sB + bs * kBTile, bb = b_full + 8 * bs;
+            const int col = (kr * 4 + kb) * 64;
+            // rows past the expert's (other experts' rows, or zeros past the
+            // end) only feed columns that are never stored
+            mbar_expect_tx(bb, (uint32_t)kBTile);
+            tma_load_2d(dst, &a.tm_b, col, jb.off + jb.n0, bb);
+            ++bcnt;
+          }
+        }
+        if (!ok) *abort_flag = 1;
+      }
+      __syncwarp();
+    }
+  } else if (warp == 9) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      int acnt = 0, bcnt = 0, jcnt = 0;
+      for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
+        const Job jb = job_of(j);
+        const int ab = jcnt & 1;
+        if (!mbar_wait_bounded(acc_empty + 8 * ab, ((jcnt >> 1) & 1) ^ 1, a.status)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t idesc = idesc_f16(kBM, jb.np);
+        const int nkb = k_of(jb) / 64;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int as = acnt % kASt, bs = bcnt % kBSt;
+          ok = mbar_wait_bounded(a_full + 8 * as, (acnt / kASt) & 1, a.status) &&
+               mbar_wait_bounded(b_full + 8 * bs, (bcnt / kBSt) & 1, a.status);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = sdesc_sw128(sB + bs * kBTile + kk * 32);
+#pragma unroll
+            for (int m = 0; m < NM; ++m)
+              tc_mma(tmem + ab * 256 + m * 128, sdesc_sw128(sA + (as * NM + m) * kATile + kk * 32), bd, idesc,
+                     (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(a_empty + 8 * as);  // the tiles are free once these MMAs are done
+          tc_commit(b_empty + 8 * bs);
+          ++acnt;
+          ++bcnt;
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_commit(acc_full + 8 * ab);  // the job's accumulators are complete
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ================= dequantisation (128 threads) =================
+    const int wd = warp - 4;
+    const int h = lane & 1;
+    int rcnt = 0, acnt = 0;
+    for (int j = bid; j < njobs && !*abort_flag; j += G) {
+      const Job jb = job_of(j);
+      const int K = k_of(jb);
+      bool ok = true;
+      for (int kr = 0; kr < K / 256 && ok; ++kr) {
+        const int rs = rcnt % kRawSt;
+        if (!(ok = mbar_wait_bounded(raw_full + 8 * rs, (rcnt / kRawSt) & 1, a.status))) break;
+        const uint32_t st = sraw + rs * raw_bytes<GU>();
+        for (int s4 = 0; s4 < 4 && ok; ++s4) {
+          const int as = acnt % kASt;
+          if (!(ok = mbar_wait_bounded(a_empty + 8 * as, ((acnt / kASt) & 1) ^ 1, a.status))) break;
+          const int c = 2 * s4 + h;  // 32-column block of the raw stage
+#pragma unroll
+          for (int m = 0; m < NM; ++m)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int r = q * 64 + wd * 16 + (lane >> 1);
+              const uint4 cw = ld_s128(st + m * kCodeBox + r * 128 + ((c ^ (r & 7)) << 4));
+              const uint32_t sh = ld_s32(st + NM * kCodeBox + m * kScaleBox + r * 16 + (c & ~1) * 2);
+              const uint32_t s1 = (c & 1) ? (sh >> 16) : (sh & 0xFFFFu);
+              const uint32_t s2u = s1 | (s1 << 16);
+              const __half2 s2 = *reinterpret_cast<const __half2*>(&s2u);
+              uint32_t o[4][4];
+              dequant_word_h(cw.x, s2, o[0]);
+              dequant_word_h(cw.y, s2, o[1]);
+              dequant_word_h(cw.z, s2, o[2]);
+              dequant_word_h(cw.w, s2, o[3]);
+              const uint32_t at = sA + (as * NM + m) * kATile + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                st_s128(at + ((((h << 2) + i) ^ (r & 7)) << 4), o[i][0], o[i][1], o[i][2], o[i][3]);
+            }
+          fence_proxy_async_shared();  // the MMA reads the tile through the async proxy
+          mbar_arrive(a_full + 8 * as);
+          ++acnt;
+        }
+        mbar_arrive(raw_empty + 8 * rs);
+        ++rcnt;
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else {
+    // ================= epilogue (warps 0-3: TMEM lanes 32w..32w+31) =================
+    const int row = warp * 32 + lane;
+    int jcnt = 0;
+    for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
+      const Job jb = job_of(j);
+      const int ab = jcnt & 1;
+      // per-column data, fetched while the job's MMAs run: the x prescale of the
+      // column's token (gate/up) or the routing weight of its pair (down)
+      float* colf = s_colf[ab];
+      if (row < jb.nn) {
+        const int s = jb.off + jb.n0 + row;
+        if (GU) colf[row] = jb.sh ? __ldg(a.xscale + (s - P)) : __ldg(a.xscale + a.sorted_pair[s] / a.k);
+        else colf[row] = jb.sh ? 1.0f : __ldg(a.w + a.sorted_pair[s]);
+      }
+      named_bar_sync(1, 128);
+      if (!mbar_wait_bounded(acc_full + 8 * ab, (jcnt >> 1) & 1, a.status)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + ab * 256;
+      bool range_ok = true;
+      for (int c0 = 0; c0 < jb.np; c0 += 16) {
+        uint32_t g[16], u[16];
+        tc_ld16(tb + c0, g);
+        if (GU) tc_ld16(tb + 128 + c0, u);
+        tc_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int n = c0 + i;
+          if (n < jb.nn) {
+            const size_t s = (size_t)jb.off + jb.n0 + n;
+            if (GU) {  // undo the token's power-of-two prescale of x (exact)
+              const float xs = colf[n];
+              const float gv = __uint_as_float(g[i]) * xs, uv = __uint_as_float(u[i]) * xs;
+              const float hv = gv / (1.0f + expf(-gv)) * uv;
+              range_ok = range_ok && fabsf(hv) < 65504.f;
+              a.h[s * a.Imax + jb.mt * kBM + row] = __half_as_ushort(__float2half_rn(hv));
+            } else {
+              a.partial[s * a.H + jb.mt * kBM + row] = colf[n] * __uint_as_float(g[i]);
+            }
+          }
+        }
+      }
+      if (!range_ok) atomicOr(a.status, DEV_RANGE);
+      tc_fence_before();
+      mbar_arrive(acc_empty + 8 * ab);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+}
+
+// Row t of x, as fp16(x[t] / 2^e_t), to every sorted row of token t (its k
+// routed pairs, pair_pos, and the shared expert's row P + t); xscale[t] = 2^e_t
+// with e_t >= 0 smallest such that max|x[t]| / 2^e_t < 2^15. Dividing a bf16
+// value by a power of two and storing it as fp16 is exact while the result
+// stays a normal fp16 number.
+__global__ void __launch_bounds__(256) x16_prep_kernel(const uint16_t* __restrict__ x, int H, int k, int P,
+                                                      const int32_t* __restrict__ pair_pos, int copies,
+                                                      uint16_t* __restrict__ x16, float* __restrict__ xscale) {
+  __shared__ float s_red[8];
+  const int t = blockIdx.x;
+  const uint16_t* xr = x + (size_t)t * H;
+  float m = 0.f;
+  for (int i = threadIdx.x; i < H; i += 256) m = fmaxf(m, fabsf(bf16_to_f(xr[i])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, s_red[i]);
+  int e = 0;
+  if (isfinite(m))
+    while (m >= 32768.f) {  // at most 113 halvings for a finite bf16 value
+      m *= 0.5f;
+      ++e;
+    }
+  const float inv = exp2f((float)-e);
+  if (threadIdx.x == 0) xscale[t] = exp2f((float)e);
+  for (int i = threadIdx.x * 8; i < H; i += 256 * 8) {  // 8 columns (16 bytes) per thread and step
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + i);
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float lo = __uint_as_float(in[q] << 16) * inv, hi = __uint_as_float(in[q] & 0xFFFF0000u) * inv;
+      const __half2 h2 = __floats2half2_rn(lo, hi);
+      o[q] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int c = 0; c < copies; ++c) {
+      const int s = c < k ? pair_pos[(size_t)t * k + c] : P + t;
+      *reinterpret_cast<uint4*>(x16 + (size_t)s * H + i) = ov;
+    }
+  }
+}
+
+}  // namespace pf
+
+// Host side -------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 pf_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+bool map2d(CUtensorMap* m, CUtensorMapDataType dt, const void* p, uint64_t inner, uint64_t rows,
+           uint64_t row_bytes, uint32_t bx, uint32_t by, bool swz) {
+  auto fn = pf_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t str[1] = {row_bytes};
+  const cuuint32_t box[2] = {bx, by};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(p), dims, str, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// codes [rows][K/2] u8: box 128 bytes (256 columns) x 128 rows, 128-byte swizzle
+bool pf_codes(CUtensorMap* m, const uint8_t* q, int K, int rows) {
+  return map2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, (uint64_t)K / 2, rows, (uint64_t)K / 2, 128, 128, true);
+}
+// scales [rows][K/32] fp16: box 8 (256 columns) x 128 rows
+bool pf_scales(CUtensorMap* m, const uint16_t* s, int K, int rows) {
+  return map2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, s, (uint64_t)K / 32, rows, (uint64_t)K / 16, 8, 128, false);
+}
+
+template <bool GU>
+cudaError_t pf_launch(pf::Args& a, cudaStream_t st) {
+  const size_t smem = pf::smem_bytes<GU>();
+  static std::mutex mu;
+  static bool configured = false;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!configured) {
+      cudaError_t e = cudaFuncSetAttribute(pf::pf_kernel<GU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e;
+      }
+      configured = true;
+    }
+  }
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  launch_begin(GU ? K_GATEUP : K_DOWN, st);
+  pf::pf_kernel<GU><<<sms > 0 ? sms : 1, pf::kThreads, smem, st>>>(a);
+  launch_end(st);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_tc_supported(int H, int I, int shI, int T, bool x_bf16) {
+  if (!x_bf16 || T <= 16) return false;
+  if (H % 256 || I % 256 || shI % 256) return false;
+  return pf_encode_fn() != nullptr;
+}
+
+cudaError_t launch_ffn_prefill_tc(const FfnArgs& f, const void* x, cudaStream_t st) {
+  const int H = f.H, I = f.I, shI = f.shI, S = f.S;
+  const int rows = f.P + f.T;
+  // the expert-sorted fp16 x lives in the partial buffer: only the down kernel,
+  // which runs after the gate/up kernel, writes partials
+  uint16_t* x16s = reinterpret_cast<uint16_t*>(f.partial);
+  pf::Args g;
+  std::memset(&g, 0, sizeof g);
+  g.H = H; g.I = I; g.shI = shI; g.k = f.k; g.T = f.T; g.P = f.P; g.Imax = f.Imax;
+  g.act = f.act; g.counters = f.counters; g.sorted_pair = f.sorted_pair; g.w = f.w;
+  g.h = f.hhi; g.partial = f.partial; g.status = f.status;
+  g.xscale = f.xcorr;
+  pf::Args d = g;
+  bool ok = pf_codes(&g.tm_c[0], f.gq, H, S * I) && pf_codes(&g.tm_c[1], f.uq, H, S * I) &&
+            pf_scales(&g.tm_s[0], f.gs, H, S * I) && pf_scales(&g.tm_s[1], f.us, H, S * I) &&
+            map2d(&g.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16s, H, rows, (uint64_t)H * 2, 64, pf::kNT, true) &&
+            pf_codes(&d.tm_c[0], f.dq, I, S * H) && pf_scales(&d.tm_s[0], f.ds, I, S * H) &&
+            map2d(&d.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, f.hhi, f.Imax, rows, (uint64_t)f.Imax * 2, 64,
+                  pf::kNT, true);
+  if (ok && shI > 0)
+    ok = pf_codes(&g.tm_sc[0], f.sgq, H, shI) && pf_codes(&g.tm_sc[1], f.suq, H, shI) &&
+         pf_scales(&g.tm_ss[0], f.sgs, H, shI) && pf_scales(&g.tm_ss[1], f.sus, H, shI) &&
+         pf_codes(&d.tm_sc[0], f.sdq, shI, H) && pf_scales(&d.tm_ss[0], f.sds, shI, H);
+  if (!ok) return cudaErrorInvalidValue;
+  launch_begin(K_X_PREP, st);
+  pf::x16_prep_kernel<<<f.T, 256, 0, st>>>(static_cast<const uint16_t*>(x), H, f.k, f.P, f.pair_pos,
+                                           f.k + (shI > 0 ? 1 : 0), x16s, const_cast<float*>(f.xcorr));
+  launch_end(st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = pf_launch<true>(g, st);
+  if (e != cudaSuccess) return e;
+  return pf_launch<false>(d, st);
+}
+
+}  // namespace moe
