@@ -153,6 +153,27 @@ __device__ __forceinline__ bool mbar_try_wait_ns(uint32_t bar, uint32_t parity, 
   return ok != 0;
 }
 
+// Bounded wait that sleeps in the barrier (up to ~hint_ns per try) instead of
+// spinning: for warps that wait often, so that waiting leaves the issue slots
+// to the warps that compute. Gives up after about a second (DEV_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, int32_t* status,
+                                                uint32_t hint_ns = 1000) {
+  if (mbar_try_wait_ns(bar, parity, hint_ns)) return true;
+  const long long t0 = cycles_now();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_ns(bar, parity, hint_ns)) return true;
+    if ((it & 15) == 0 && cycles_now() - t0 > kWaitCycles) {
+      if (status) atomicOr(status, DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Bounded wait with a short sleep per try (for waits on fast pipeline stages).
+__device__ __forceinline__ bool mbar_wait_short(uint32_t bar, uint32_t parity, int32_t* status) {
+  return mbar_wait_sleep(bar, parity, status, 128);
+}
+
 // f = (a & b) ^ c
 __device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;

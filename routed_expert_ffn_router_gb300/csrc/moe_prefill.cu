@@ -9,13 +9,15 @@
 // permutation: an expert's tokens are consecutive rows of the sorted order.
 //
 // Two persistent kernels, one per GEMM, each a warp-specialised pipeline:
-//   warp 8 (one thread) streams a job's int4 codes and fp16 scales (TMA tensor
-//   copies, 256 columns of K per raw stage) and its B operand (64 columns of K
-//   per stage, one TMA box of its rows of the expert-sorted x or h);
-//   warps 4-7 dequantise a raw stage into fp16 A tiles (128 rows x 64, K-major,
+//   warp 12 (one thread) streams a job's int4 codes and fp16 scales (TMA tensor
+//   copies, 256 columns of K per raw stage), warp 13 (one thread) its B
+//   operand (TMA boxes of its rows of the expert-sorted x or h, 64 columns of
+//   K each; a 16 KB B slot holds 1, 2, 4 or 8 of them for 128, 64, 32 or 16
+//   rows, so that jobs with few tokens keep more of K in flight);
+//   warps 4-11 dequantise a raw stage into fp16 A tiles (128 rows x 64, K-major,
 //   128-byte swizzle): q = (1024 + (q ^ 8)) - 1032 exactly, then q * s with the
 //   fp16 scale, rounded once (2^-12);
-//   warp 9 (one thread) issues tcgen05.mma (M = 128, N = the job's tokens
+//   warp 14 (one thread) issues tcgen05.mma (M = 128, N = the job's tokens
 //   rounded up to 16, K = 16 per instruction) into one of two TMEM buffers and
 //   commits each stage back to its producers;
 //   warps 0-3 (one TMEM lane quarter each) drain the accumulators: h =
@@ -26,7 +28,8 @@
 // order (x16_prep_kernel; e_t is the smallest power of two that keeps the row
 // below 2^15, 0 for ordinary activations): exact for every bf16 value in
 // range, and the gate/up epilogue multiplies g and u back by 2^e_t.
-// A job is (active expert, 128 weight rows, up to 128 of its tokens); CTA b
+// A job is (active expert, 128 gate and 128 up rows, or 256 down rows, up to
+// 128 of its tokens); CTA b
 // takes jobs b, b + G, ... of the list both kernels derive from the
 // permutation. The ordered combine (moe_decode.cu) then sums the partials in
 // j order and adds the shared expert, which enters as one more expert with all
@@ -45,7 +48,8 @@ namespace pf {
 constexpr int kBM = 128;              // weight rows per job (M of the MMA)
 constexpr int kNT = 128;              // tokens per job at most (N of the MMA)
 constexpr int kRawSt = 2, kASt = 2, kBSt = 4;
-constexpr int kThreads = 320;         // warps 0-3 epilogue, 4-7 dequant, 8 producer, 9 MMA
+constexpr int kThreads = 480;         // warps 0-3 epilogue, 4-11 dequant, 12-13 producers, 14 MMA
+constexpr int kDq = 256;              // dequantising threads
 constexpr int kMaxAct = kMaxE + 1;
 constexpr int kCodeBox = 128 * 128;   // one raw code box: 128 rows x 128 bytes (256 columns)
 constexpr int kScaleBox = 128 * 16;   // one raw scale box: 128 rows x 8 fp16
@@ -55,7 +59,8 @@ constexpr int kBTile = kNT * 128;     // one fp16 B tile: up to 128 rows x 64 co
 struct Args {
   CUtensorMap tm_c[2], tm_s[2];       // routed codes / scales (gate, up; or down)
   CUtensorMap tm_sc[2], tm_ss[2];     // the shared expert's
-  CUtensorMap tm_b;                   // expert-sorted x16 [rows][H] or h [rows][Imax], fp16
+  CUtensorMap tm_b[4];                // expert-sorted x16 [rows][H] or h [rows][Imax], fp16,
+                                      // boxes of 16, 32, 64 and 128 rows
   int H, I, shI, k, T, P, Imax;
   const ActExpert* act;
   const int32_t* counters;            // [0]: active experts including the shared one
@@ -67,8 +72,11 @@ struct Args {
   int32_t* status;
 };
 
+// Two A tiles per stage: gate and up (gate/up), or two row tiles (down).
 template <bool GU>
-__host__ __device__ constexpr int nmat() { return GU ? 2 : 1; }
+__host__ __device__ constexpr int nmat() { return 2; }
+template <bool GU>
+__host__ __device__ constexpr int job_rows() { return GU ? kBM : 2 * kBM; }
 template <bool GU>
 __host__ __device__ constexpr int raw_bytes() { return nmat<GU>() * (kCodeBox + kScaleBox); }
 template <bool GU>
@@ -127,6 +135,7 @@ __device__ __forceinline__ void dequant_word_h(uint32_t wd, __half2 s2, uint32_t
 
 struct Job {
   int a, mt, n0, nn, np;   // active entry, row tile, first token slot, tokens, tokens rounded to 16
+  int bsel;                // B box of 16 << bsel rows; a B slot holds 8 >> bsel boxes
   int off, slot;           // first sorted row of the expert; pool slot (-1: shared)
   bool sh;
 };
@@ -160,10 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     s_abort = 0;
     for (int i = 0; i < kRawSt; ++i) {
       mbar_init(raw_full + 8 * i, 1);
-      mbar_init(raw_empty + 8 * i, 128);
+      mbar_init(raw_empty + 8 * i, kDq / 32);  // one arrival per dequantising warp
     }
     for (int i = 0; i < kASt; ++i) {
-      mbar_init(a_full + 8 * i, 128);
+      mbar_init(a_full + 8 * i, kDq / 32);
       mbar_init(a_empty + 8 * i, 1);
     }
     for (int i = 0; i < kBSt; ++i) {
@@ -172,11 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(acc_full + 8 * i, 1);
-      mbar_init(acc_empty + 8 * i, 128);
+      mbar_init(acc_empty + 8 * i, 4);
     }
     fence_barrier_init();
   }
-  if (warp == 9) {  // the whole TMEM (512 columns): two accumulator buffers of 256
+  if (warp == 14) {  // the whole TMEM (512 columns): two accumulator buffers of 256
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&s_tmem)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
@@ -195,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     int sum = 0;
     for (int i = i0; i < i1; ++i) {
       const int rows = GU ? (s_slot[i] < 0 ? a.shI : a.I) : a.H;
-      sum += (rows / kBM) * ((s_cnt[i] + kNT - 1) / kNT);
+      sum += (rows / job_rows<GU>()) * ((s_cnt[i] + kNT - 1) / kNT);
     }
     int x = sum;
 #pragma unroll
@@ -207,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     for (int i = i0; i < i1; ++i) {
       s_js[i] = run;
       const int rows = GU ? (s_slot[i] < 0 ? a.shI : a.I) : a.H;
-      run += (rows / kBM) * ((s_cnt[i] + kNT - 1) / kNT);
+      run += (rows / job_rows<GU>()) * ((s_cnt[i] + kNT - 1) / kNT);
     }
     if (lane == 31) s_js[n_act] = x;
   }
@@ -228,89 +237,113 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     jb.a = lo;
     jb.sh = s_slot[lo] < 0;
     const int rows = GU ? (jb.sh ? a.shI : a.I) : a.H;
-    const int nM = rows / kBM;
+    const int nM = rows / job_rows<GU>();
     const int loc = j - s_js[lo];
     jb.mt = loc % nM;
     jb.n0 = (loc / nM) * kNT;
     jb.nn = min(kNT, s_cnt[lo] - jb.n0);
     jb.np = (jb.nn + 15) & ~15;
+    jb.bsel = jb.np <= 16 ? 0 : jb.np <= 32 ? 1 : jb.np <= 64 ? 2 : 3;
     jb.off = s_off[lo];
     jb.slot = s_slot[lo];
     return jb;
   };
   auto k_of = [&](const Job& jb) { return GU ? a.H : (jb.sh ? a.shI : a.I); };
 
-  if (warp == 8) {
-    // ================= producer =================
-    int rcnt = 0, bcnt = 0;
-    const uint64_t wpol = l2_evict_first_policy();
-    for (int j = bid; j < njobs && !*abort_flag; j += G) {
-      const Job jb = job_of(j);
-      if (lane == 0) {
+  if (warp == 12) {
+    // ================= raw producer: codes and scales =================
+    if (lane == 0) {
+      int rcnt = 0;
+      for (int j = bid; j < njobs && !*abort_flag; j += G) {
+        const Job jb = job_of(j);
         const int K = k_of(jb);
-        const int row0 = (jb.sh ? 0 : jb.slot * (GU ? a.I : a.H)) + jb.mt * kBM;
+        const int row0 = (jb.sh ? 0 : jb.slot * (GU ? a.I : a.H)) + jb.mt * job_rows<GU>();
         bool ok = true;
-        for (int kr = 0; kr < K / 256 && ok; ++kr) {
+        for (int kr = 0; kr < K / 256; ++kr) {
           const int rs = rcnt % kRawSt;
-          if (!(ok = mbar_wait_bounded(raw_empty + 8 * rs, ((rcnt / kRawSt) & 1) ^ 1, a.status))) break;
+          if (!(ok = mbar_wait_short(raw_empty + 8 * rs, ((rcnt / kRawSt) & 1) ^ 1, a.status))) break;
           const uint32_t st = sraw + rs * raw_bytes<GU>(), fb = raw_full + 8 * rs;
           mbar_expect_tx(fb, raw_bytes<GU>());
 #pragma unroll
-          for (int m = 0; m < NM; ++m) {
-            tma_load_2d_hint(st + m * kCodeBox, jb.sh ? &a.tm_sc[m] : &a.tm_c[m], kr * 128, row0, fb, wpol);
-            tma_load_2d_hint(st + NM * kCodeBox + m * kScaleBox, jb.sh ? &a.tm_ss[m] : &a.tm_s[m], kr * 8,
-                             row0, fb, wpol);
+          for (int m = 0; m < NM; ++m) {  // gate/up: two matrices; down: two row tiles of one
+            const int mi = GU ? m : 0, rm = GU ? row0 : row0 + m * kBM;
+            tma_load_2d(st + m * kCodeBox, jb.sh ? &a.tm_sc[mi] : &a.tm_c[mi], kr * 128, rm, fb);
+            tma_load_2d(st + NM * kCodeBox + m * kScaleBox, jb.sh ? &a.tm_ss[mi] : &a.tm_s[mi], kr * 8, rm,
+                        fb);
           }
           ++rcnt;
-          for (int kb = 0; kb < 4 && ok; ++kb) {
-            const int bs = bcnt % kBSt;
-            if (!(ok = mbar_wait_bounded(b_empty + 8 * bs, ((bcnt / kBSt) & 1) ^ 1, a.status))) break;
-            const uint32_t dst = sB + bs * kBTile, bb = b_full + 8 * bs;
-            const int col = (kr * 4 + kb) * 64;
-            // rows past the expert's (other experts' rows, or zeros past the
-            // end) only feed columns that are never stored
-            mbar_expect_tx(bb, (uint32_t)kBTile);
-            tma_load_2d(dst, &a.tm_b, col, jb.off + jb.n0, bb);
-            ++bcnt;
-          }
         }
-        if (!ok) *abort_flag = 1;
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
       }
-      __syncwarp();
     }
-  } else if (warp == 9) {
+    __syncwarp();
+  } else if (warp == 13) {
+    // ================= B producer: expert-sorted rows of x or h =================
+    if (lane == 0) {
+      int bcnt = 0;
+      for (int j = bid; j < njobs && !*abort_flag; j += G) {
+        const Job jb = job_of(j);
+        const uint32_t bbytes = (16u << jb.bsel) * 128;  // one box
+        const int spb = 8 >> jb.bsel;                      // boxes per slot
+        bool ok = true;
+        for (int kb = 0; kb < k_of(jb) / 64; kb += spb) {
+          const int bs = bcnt % kBSt;
+          if (!(ok = mbar_wait_short(b_empty + 8 * bs, ((bcnt / kBSt) & 1) ^ 1, a.status))) break;
+          const uint32_t dst = sB + bs * kBTile, bb = b_full + 8 * bs;
+          // rows past the expert's (other experts' rows, or zeros past the end)
+          // only feed columns that are never stored
+          mbar_expect_tx(bb, bbytes * spb);
+          for (int u = 0; u < spb; ++u)
+            tma_load_2d(dst + u * bbytes, &a.tm_b[jb.bsel], (kb + u) * 64, jb.off + jb.n0, bb);
+          ++bcnt;
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 14) {
     // ================= MMA issuer =================
     if (lane == 0) {
       int acnt = 0, bcnt = 0, jcnt = 0;
       for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
         const Job jb = job_of(j);
         const int ab = jcnt & 1;
-        if (!mbar_wait_bounded(acc_empty + 8 * ab, ((jcnt >> 1) & 1) ^ 1, a.status)) {
+        if (!mbar_wait_short(acc_empty + 8 * ab, ((jcnt >> 1) & 1) ^ 1, a.status)) {
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
         const uint32_t idesc = idesc_f16(kBM, jb.np);
         const int nkb = k_of(jb) / 64;
+        const int spb = 8 >> jb.bsel;
+        const uint32_t bbytes = (16u << jb.bsel) * 128;
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
-          const int as = acnt % kASt, bs = bcnt % kBSt;
-          ok = mbar_wait_bounded(a_full + 8 * as, (acnt / kASt) & 1, a.status) &&
-               mbar_wait_bounded(b_full + 8 * bs, (bcnt / kBSt) & 1, a.status);
+          const int as = acnt % kASt, bs = bcnt % kBSt, u = kb % spb;
+          ok = mbar_wait_short(a_full + 8 * as, (acnt / kASt) & 1, a.status) &&
+               (u != 0 || mbar_wait_short(b_full + 8 * bs, (bcnt / kBSt) & 1, a.status));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sdesc_sw128(sB + bs * kBTile + kk * 32);
+            const uint64_t bd = sdesc_sw128(sB + bs * kBTile + u * bbytes + kk * 32);
 #pragma unroll
             for (int m = 0; m < NM; ++m)
               tc_mma(tmem + ab * 256 + m * 128, sdesc_sw128(sA + (as * NM + m) * kATile + kk * 32), bd, idesc,
                      (kb > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(a_empty + 8 * as);  // the tiles are free once these MMAs are done
-          tc_commit(b_empty + 8 * bs);
           ++acnt;
-          ++bcnt;
+          if (u == spb - 1) {
+            tc_commit(b_empty + 8 * bs);
+            ++bcnt;
+          }
         }
         if (!ok) {
           *abort_flag = 1;
@@ -321,8 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ================= dequantisation (128 threads) =================
-    const int wd = warp - 4;
+    // ================= dequantisation (warps 4-11: matrix or row tile m = wd / 4) =================
+    const int wd = warp - 4, m = wd >> 2;
     const int h = lane & 1;
     int rcnt = 0, acnt = 0;
     for (int j = bid; j < njobs && !*abort_flag; j += G) {
@@ -331,17 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       bool ok = true;
       for (int kr = 0; kr < K / 256 && ok; ++kr) {
         const int rs = rcnt % kRawSt;
-        if (!(ok = mbar_wait_bounded(raw_full + 8 * rs, (rcnt / kRawSt) & 1, a.status))) break;
+        if (!(ok = mbar_wait_short(raw_full + 8 * rs, (rcnt / kRawSt) & 1, a.status))) break;
         const uint32_t st = sraw + rs * raw_bytes<GU>();
         for (int s4 = 0; s4 < 4 && ok; ++s4) {
           const int as = acnt % kASt;
-          if (!(ok = mbar_wait_bounded(a_empty + 8 * as, ((acnt / kASt) & 1) ^ 1, a.status))) break;
+          if (!(ok = mbar_wait_short(a_empty + 8 * as, ((acnt / kASt) & 1) ^ 1, a.status))) break;
           const int c = 2 * s4 + h;  // 32-column block of the raw stage
 #pragma unroll
-          for (int m = 0; m < NM; ++m)
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const int r = q * 64 + wd * 16 + (lane >> 1);
+          for (int q = 0; q < 2; ++q) {
+              const int r = q * 64 + (wd & 3) * 16 + (lane >> 1);
               const uint4 cw = ld_s128(st + m * kCodeBox + r * 128 + ((c ^ (r & 7)) << 4));
               const uint32_t sh = ld_s32(st + NM * kCodeBox + m * kScaleBox + r * 16 + (c & ~1) * 2);
               const uint32_t s1 = (c & 1) ? (sh >> 16) : (sh & 0xFFFFu);
@@ -358,10 +389,12 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
                 st_s128(at + ((((h << 2) + i) ^ (r & 7)) << 4), o[i][0], o[i][1], o[i][2], o[i][3]);
             }
           fence_proxy_async_shared();  // the MMA reads the tile through the async proxy
-          mbar_arrive(a_full + 8 * as);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(a_full + 8 * as);
           ++acnt;
         }
-        mbar_arrive(raw_empty + 8 * rs);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(raw_empty + 8 * rs);
         ++rcnt;
       }
       if (!ok) *abort_flag = 1;
@@ -382,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
         else colf[row] = jb.sh ? 1.0f : __ldg(a.w + a.sorted_pair[s]);
       }
       named_bar_sync(1, 128);
-      if (!mbar_wait_bounded(acc_full + 8 * ab, (jcnt >> 1) & 1, a.status)) {
+      if (!mbar_wait_short(acc_full + 8 * ab, (jcnt >> 1) & 1, a.status)) {
         *abort_flag = 1;
         break;
       }
@@ -390,9 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + ab * 256;
       bool range_ok = true;
       for (int c0 = 0; c0 < jb.np; c0 += 16) {
-        uint32_t g[16], u[16];
+        uint32_t g[16], u[16];  // gate/up: gate, up; down: row tiles 0 and 1
         tc_ld16(tb + c0, g);
-        if (GU) tc_ld16(tb + 128 + c0, u);
+        tc_ld16(tb + 128 + c0, u);
         tc_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -406,20 +439,23 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
               range_ok = range_ok && fabsf(hv) < 65504.f;
               a.h[s * a.Imax + jb.mt * kBM + row] = __half_as_ushort(__float2half_rn(hv));
             } else {
-              a.partial[s * a.H + jb.mt * kBM + row] = colf[n] * __uint_as_float(g[i]);
+              float* pp = a.partial + s * a.H + jb.mt * (2 * kBM) + row;
+              pp[0] = colf[n] * __uint_as_float(g[i]);
+              pp[kBM] = colf[n] * __uint_as_float(u[i]);
             }
           }
         }
       }
       if (!range_ok) atomicOr(a.status, DEV_RANGE);
       tc_fence_before();
-      mbar_arrive(acc_empty + 8 * ab);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty + 8 * ab);
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+  if (warp == 14) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
 }
 
 // Row t of x, as fp16(x[t] / 2^e_t), to every sorted row of token t (its k
@@ -510,6 +546,14 @@ bool pf_scales(CUtensorMap* m, const uint16_t* s, int K, int rows) {
   return map2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, s, (uint64_t)K / 32, rows, (uint64_t)K / 16, 8, 128, false);
 }
 
+// fp16 [rows][cols] B operand: boxes of 64 columns x 16, 32, 64 and 128 rows
+bool b_maps(CUtensorMap* m, const void* p, int cols, int rows) {
+  for (int i = 0; i < 4; ++i)
+    if (!map2d(&m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p, cols, rows, (uint64_t)cols * 2, 64, 16u << i, true))
+      return false;
+  return true;
+}
+
 template <bool GU>
 cudaError_t pf_launch(pf::Args& a, cudaStream_t st) {
   const size_t smem = pf::smem_bytes<GU>();
@@ -539,7 +583,7 @@ cudaError_t pf_launch(pf::Args& a, cudaStream_t st) {
 
 bool prefill_tc_supported(int H, int I, int shI, int T, bool x_bf16) {
   if (!x_bf16 || T <= 16) return false;
-  if (H % 256 || I % 256 || shI % 256) return false;
+  if (H % 256 || I % 256 || shI % 256) return false;  // raw stages of 256 columns, down jobs of 256 rows
   return pf_encode_fn() != nullptr;
 }
 
@@ -558,10 +602,9 @@ cudaError_t launch_ffn_prefill_tc(const FfnArgs& f, const void* x, cudaStream_t 
   pf::Args d = g;
   bool ok = pf_codes(&g.tm_c[0], f.gq, H, S * I) && pf_codes(&g.tm_c[1], f.uq, H, S * I) &&
             pf_scales(&g.tm_s[0], f.gs, H, S * I) && pf_scales(&g.tm_s[1], f.us, H, S * I) &&
-            map2d(&g.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16s, H, rows, (uint64_t)H * 2, 64, pf::kNT, true) &&
+            b_maps(g.tm_b, x16s, H, rows) &&
             pf_codes(&d.tm_c[0], f.dq, I, S * H) && pf_scales(&d.tm_s[0], f.ds, I, S * H) &&
-            map2d(&d.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, f.hhi, f.Imax, rows, (uint64_t)f.Imax * 2, 64,
-                  pf::kNT, true);
+            b_maps(d.tm_b, f.hhi, f.Imax, rows);
   if (ok && shI > 0)
     ok = pf_codes(&g.tm_sc[0], f.sgq, H, shI) && pf_codes(&g.tm_sc[1], f.suq, H, shI) &&
          pf_scales(&g.tm_ss[0], f.sgs, H, shI) && pf_scales(&g.tm_ss[1], f.sus, H, shI) &&
