@@ -395,9 +395,11 @@ struct Producer {
   int4* hdr;
   const int32_t* act_slot;
   int D;
+  int nst, stage_bytes;
   uint64_t wpol;   // L2 policy of the weight copies
   int j;           // jobs issued
   int ui, pd;      // units taken, units published
+  int slot, phase; // ring position of job j (slot = j mod nst, phase = (j / nst) & 1)
 
   // Publish the units whose partials are all stored (never blocks).
   __device__ __forceinline__ void poll() {
@@ -415,9 +417,8 @@ struct Producer {
   // Free slot for job j (publishing meanwhile).
   // The thread sleeps in the barrier wait between polls: a spinning producer
   // would take issue slots from the consumer warps of its SM sub-partition.
-  __device__ __forceinline__ bool acquire_slot(int& slot) {
-    slot = j % a.nst;
-    const uint32_t par = ((j / a.nst) & 1) ^ 1;
+  __device__ __forceinline__ bool acquire_slot() {
+    const uint32_t par = phase ^ 1;
     if (mbar_test(empty0 + 8 * slot, par)) return true;
     const long long t0 = cycles_now();
     for (uint32_t it = 1;; ++it) {
@@ -432,12 +433,15 @@ struct Producer {
   }
   __device__ __forceinline__ bool issue(int kind, int d, int grp, int chunk) {
     constexpr int UI = 32 * MT;
-    poll();
-    int slot;
-    if (!acquire_slot(slot)) return false;
+    if ((j & 3) == 0) poll();  // publications are also handled whenever the producer waits
+    if (!acquire_slot()) return false;
     hdr[slot] = make_int4(kind, d, grp, chunk);
-    const uint32_t st = sbase + slot * a.stage_bytes, fb = full0 + 8 * slot;
+    const uint32_t st = sbase + slot * stage_bytes, fb = full0 + 8 * slot;
     ++j;
+    if (++slot == nst) {
+      slot = 0;
+      phase ^= 1;
+    }
     if (kind == J_END) {
       mbar_arrive(fb);
       return true;
@@ -653,8 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     if (lane == 0) {
       // ================= producer (one thread) =================
       fence_proxy_async_shared();  // the top-k scratch in stage memory precedes the TMA writes
-      Producer<MT> P{a, sbase, full0, empty0, pub0, s_hdr, s_act_slot, D,
-                     l2_evict_first_policy(), 0, 0, 0};
+      Producer<MT> P{a, sbase, full0, empty0, pub0, s_hdr, s_act_slot, D, a.nst, a.stage_bytes,
+                     l2_evict_first_policy(), 0, 0, 0, 0, 0};
       bool ok = true;
       bool w_pub = !(layer_mode && bid < T);
       int next = ticket;
@@ -712,10 +716,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     int browx[2] = {0, 0};  // x box row (token) of token slot nt*8 + g
     int browh[2] = {0, 0};  // h buffer row (slot) of token slot nt*8 + g
     int cnt = 0, ntiles = 1, ucnt = 0;
-    for (int j = 0;; ++j) {
+    const int nst = a.nst;
+    int slot = 0, phase = 0, cslot = -1;  // ring position of the job being consumed
+    for (;;) {
+      if (cslot >= 0 && ++slot == nst) {  // advance past the previous job
+        slot = 0;
+        phase ^= 1;
+      }
+      cslot = slot;
       if (*abort_flag) break;
-      const int slot = j % a.nst;
-      if (!mbar_wait_bounded(full0 + 8 * slot, (j / a.nst) & 1, a.status)) {
+      if (!mbar_wait_bounded(full0 + 8 * slot, phase, a.status)) {
         *abort_flag = 1;
         break;
       }
