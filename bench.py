@@ -48,6 +48,9 @@ def parse():
                     help="skip the secondary configurations (prefill, 48-layer decode, expert cache)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="bound on the oracle's CPU time for cpu_baseline")
+    ap.add_argument("--profile-case", choices=["decode_window", "prefill"], default=None,
+                    help="run a few eager launches of one small case and exit (the target "
+                         "of ncu captures: about 1 GB on the device, inputs larger than L2)")
     return ap.parse_args()
 
 
@@ -98,17 +101,71 @@ def _cuda_ok():
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """SM clock and clock-event (throttle) reasons sampled while the timed region runs.
+
+    Reads NVML in-process (ctypes on the driver's libnvidia-ml) from a thread
+    every ~0.5 ms, so that even a few-millisecond timed region gets samples;
+    falls back to `nvidia-smi -lms 100`. Read-only queries: no setting changes.
+    """
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, pci_bus_id: str = ""):
         self.gpu = gpu_index
+        self.pci = pci_bus_id
         self.proc = None
+        self.thread = None
+        self.samples = []
         self.out = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
 
+    def _nvml(self):
+        import ctypes
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                lib = None
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        # The CUDA device's own PCI id: NVML indices need not follow CUDA's.
+        if self.pci and lib.nvmlDeviceGetHandleByPciBusId_v2(self.pci.encode(), ctypes.byref(h)) == 0:
+            return lib, h
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+            return None
+        return lib, h
+
     def start(self):
+        import threading
+        nv = self._nvml()
+        if nv is not None:
+            import ctypes
+            lib, h = nv
+            self.stop_flag = False
+            mx = ctypes.c_uint(0)
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+
+            began = threading.Event()
+
+            def run():
+                clk, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+                while not self.stop_flag:
+                    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                            get_reasons(h, ctypes.byref(rs)) == 0:
+                        self.samples.append((clk.value, rs.value))
+                    began.set()
+                    time.sleep(0.0005)
+            self.thread = threading.Thread(target=run, daemon=True)
+            self.thread.start()
+            began.wait(1.0)
+            return
         try:
             self.f = open(self.out, "w")
             self.proc = subprocess.Popen(
@@ -118,6 +175,13 @@ class ClockSampler:
             self.proc = None
 
     def stop(self) -> dict:
+        if self.thread is not None:
+            self.stop_flag = True
+            self.thread.join(2)
+            sm = [c for c, _ in self.samples]
+            reasons = sorted({n for _, r in self.samples for b, n in self.REASONS.items() if r & b})
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(sm), "source": "nvml"}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -143,7 +207,16 @@ class ClockSampler:
         os.unlink(self.out)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi"}
+
+
+def pci_id(torch, dev: int) -> str:
+    """domain:bus:device.0 of a CUDA device, as NVML expects it ("" if unknown)."""
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except Exception:
+        return ""
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -290,7 +363,7 @@ def run_ours(args, dist):
     for _ in range(2):  # graph warm-up
         time_graph(torch, graphs, min(reps, len(graphs)), stream)
 
-    clocks = ClockSampler(dist.local)
+    clocks = ClockSampler(dist.local, pci_id(torch, torch.cuda.current_device()))
     dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
@@ -523,6 +596,55 @@ def extra_configs(torch, synth, _lib, dev, stream, hbm_peak, tf_peak):
     return out
 
 
+# ----------------------------------------------------------------------------- profiling
+def run_profile_case(case: str):
+    """Eager launches for an ncu capture: decode_window = 6 windows over 2 pool
+    copies (0.7 GB of weights, > L2); prefill = 4 passes of the 2,048-token
+    chunk (0.9 GB of weights). Prints the per-kernel times of the library's
+    own event timing for the last passes."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from routed_expert_ffn_router_gb300 import _lib, synth
+    from routed_expert_ffn_router_gb300.layer import MoeLayer
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    dev = torch.device("cuda", 0)
+    if case == "decode_window":
+        wl = DecodeWindowWorkload(torch, synth, synth.DECODE_WINDOW, dev, n_pools=2, n_windows=4)
+        fn = wl.step
+        n = 6
+        lay = wl.layers[0]
+    else:
+        cfg = synth.PREFILL
+        inp = synth.make_layer(cfg, 0, device=dev)
+        lay = MoeLayer(inp, T_max=cfg.T)
+        out = lay.alloc_outputs(cfg.T)
+
+        def fn(i):
+            lay.forward(inp.logits, inp.x, out=out)
+        n = 4
+    for i in range(n - 2):
+        fn(i)
+    torch.cuda.synchronize()
+    _lib.moe_profile_enable(1000)
+    for i in range(n - 2, n):
+        fn(i)
+    torch.cuda.synchronize()
+    _lib.moe_profile_collect()
+    tot = _lib.moe_profile_totals()
+    _lib.moe_profile_enable(0)
+    code, bits = lay.status()
+    assert code == _lib.MOE_OK, f"device status {bits}"
+    for k, (ms, cnt) in sorted(tot.items(), key=lambda kv: -kv[1][0]):
+        if cnt:
+            print(f"{k:16s} {ms / cnt * 1e3:9.2f} us/launch  launches {cnt}")
+    if case == "decode_window":
+        wl.count_distinct(torch)
+        for i in range(n):
+            print(f"step {i}: distinct experts {wl.distinct[i % wl.n_windows]}, "
+                  f"algorithmic bytes {wl.step_bytes(i)}")
+
+
 # ----------------------------------------------------------------------------- reference
 def run_reference(args, dist):
     """The CPU oracle as the reference arm: one sampled row of a decode window
@@ -574,6 +696,9 @@ def run_reference(args, dist):
 
 def main():
     args = parse()
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
     dist = Dist()
     try:
         if args.impl == "reference":
