@@ -45,7 +45,9 @@ namespace moe {
 namespace fused {
 
 constexpr int kCW = 8;                  // consumer warps: 4 row warps x 2 column halves
-constexpr int kThreads = 32 * (kCW + 1);
+constexpr int kHelperWarp = kCW + 1;    // routing weights of one row, off the weight stream's path
+constexpr int kWarps = kCW + 2;         // producer, consumers, helper
+constexpr int kThreads = 32 * kWarps;
 constexpr int kKC = 256;                // columns of K per job
 constexpr int kMaxNst = 8;              // stages in the ring at most
 constexpr int kUnitRing = 16;           // units a producer may have unpublished
@@ -54,6 +56,7 @@ constexpr int kDnRows = 512;            // output rows per down job (two 256-row
 constexpr int kDnM = kDnRows / (kCW * 16);  // m16 tiles per warp in a down job
 constexpr int kPubCount = kCW * 32;     // arrivals that publish a unit (every consumer lane)
 constexpr int kPubBars = 4;             // publish barriers, used by units in turn
+constexpr int kStgRow = 68;             // floats per token row of a warp's partial staging (64 + 4 pad)
 constexpr uint32_t kBf16NegMagic = 0xC308C308u;  // bf16 -136
 constexpr uint32_t kF16NegMagic = 0xE408E408u;   // f16 -1032
 
@@ -99,14 +102,19 @@ __host__ __device__ constexpr int dn_job_bytes(int MT) { return kDnRows * 16 * M
 __host__ __device__ constexpr int stage_bytes_for(int MT, int TB) {
   return gu_job_bytes(MT, TB) > dn_job_bytes(MT) ? gu_job_bytes(MT, TB) : dn_job_bytes(MT);
 }
-__host__ __device__ constexpr int red_bytes(int MT) { return 4 * (MT * 2 * 4) * 32 * 4; }
+__host__ __device__ constexpr int red_bytes(int MT, int NTX) { return 4 * (MT * NTX * 4) * 32 * 4; }
 // two h buffers [kMaxT][UI + 8] f16 (the 16-byte pad keeps the B loads free of bank conflicts)
 __host__ __device__ constexpr int hb_bytes(int MT) { return 2 * kMaxT * (64 * MT + 16); }
+// per consumer warp, the down partials of its 64 rows: [TB][kStgRow] f32
+__host__ __device__ constexpr int stg_bytes(int TB) { return kCW * TB * kStgRow * 4; }
 // Dynamic shared memory: 1 KB of alignment slack, the stages, the exchange
-// buffer of the two column halves, the h buffers.
-__host__ __device__ inline size_t smem_bytes(int MT, int nst, int stage_bytes) {
-  return 1024 + (size_t)nst * stage_bytes + red_bytes(MT) + hb_bytes(MT);
+// buffer of the two column halves, the h buffers, the partial staging rows.
+__host__ __device__ inline size_t smem_bytes(int MT, int NTX, int nst, int stage_bytes, int TB) {
+  return 1024 + (size_t)nst * stage_bytes + red_bytes(MT, NTX) + hb_bytes(MT) + stg_bytes(TB);
 }
+// The slot map's copy lives in stage memory during the routing (after the
+// top-k scratch of every warp), before the first weight copy.
+constexpr int kSlotMapOff = 32768;
 
 __device__ __forceinline__ uint32_t order_key(float v) {
   uint32_t u = __float_as_uint(v);
@@ -480,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   __shared__ int s_ids[kMaxT][kMaxK];
   __shared__ uint32_t s_tokmask[kMaxE];
   __shared__ int16_t s_d_of_e[kMaxE];
-  __shared__ int32_t s_slot[kMaxE];
+  __shared__ float s_topv[kMaxT][kMaxK];  // the selected logits of each row, in rank order
   __shared__ int16_t s_act_e[kMaxE + 1];
   __shared__ int32_t s_act_slot[kMaxE + 1];
   __shared__ int16_t s_act_off[kMaxE + 1];
@@ -501,7 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
   const uint32_t sbase = smem_u32(smem);
   float* const red = reinterpret_cast<float*>(smem + (size_t)a.nst * a.stage_bytes);
-  uint8_t* const hbuf = smem + (size_t)a.nst * a.stage_bytes + red_bytes(MT);
+  uint8_t* const hbuf = smem + (size_t)a.nst * a.stage_bytes + red_bytes(MT, MAXNT);
+  const uint32_t stg_s = smem_u32(hbuf) + hb_bytes(MT);
+  int32_t* const s_slot = reinterpret_cast<int32_t*>(smem + kSlotMapOff);
   const uint32_t full0 = smem_u32(&s_bar[0]), empty0 = full0 + 8 * kMaxNst,
                  pub0 = empty0 + 8 * kMaxNst;
   volatile int* abort_flag = &s_abort;  // read in loops without barriers
@@ -542,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   // The stage buffers are still idle: they hold the top-k scratch.
   if (layer_mode) {
     unsigned long long* scr = reinterpret_cast<unsigned long long*>(smem) + warp * kTopkScratch;
-    for (int t = warp; t < T; t += kCW + 1) {
+    for (int t = warp; t < T; t += kWarps) {
       const float* l = a.logits + (size_t)t * E;
       bool bad;
       if (E <= 128) bad = topk_row<4>(l, E, k, scr, &s_ids[t][0]);
@@ -550,20 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
       else if (E <= 512) bad = topk_row<16>(l, E, k, scr, &s_ids[t][0]);
       else bad = topk_row<32>(l, E, k, scr, &s_ids[t][0]);
       if (bad && lane == 0 && bid == 0) atomicOr(a.status, DEV_NONFINITE_LOGIT);
-      if (bid == t) {
-        // float64 softmax over the k selected, in rank order (the ranked keys are in scr)
-        const float v = lane < k ? key_value((uint32_t)(scr[kTopkRanked + lane] >> 32)) : 0.f;
-        const double m0 = (double)__shfl_sync(0xffffffffu, v, 0);
-        const double ej = lane < k ? exp((double)v - m0) : 0.0;
-        double sum = 0.0;
-        for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ej, j);
-        if (lane < k) {
-          a.ids_out[(size_t)t * k + lane] = s_ids[t][lane];
-          a.w_out[(size_t)t * k + lane] = (float)(ej / sum);
-        }
-        // published by this CTA's producer (a gpu-scope fence is slow and the
-        // combine that reads the weights comes much later)
-      }
+      if (lane < k) s_topv[t][lane] = key_value((uint32_t)(scr[kTopkRanked + lane] >> 32));
       __syncwarp();
     }
   } else {
@@ -660,7 +657,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
       Producer<MT> P{a, sbase, full0, empty0, pub0, s_hdr, s_act_slot, D, a.nst, a.stage_bytes,
                      l2_evict_first_policy(), 0, 0, 0, 0, 0};
       bool ok = true;
-      bool w_pub = !(layer_mode && bid < T);
       int next = ticket;
       while (ok && !*abort_flag && ticket < sc.total) {
         if (P.ui - P.pd >= kUnitRing) {  // bound the unpublished units
@@ -678,18 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
         for (int ch = 0; ch < nch && ok; ++ch) ok = P.issue(J_GU, u.x, u.y, ch);
         for (int ch = 0; ch < nchd && ok; ++ch) ok = P.issue(J_DN, u.x, u.y, ch);
         ticket = next;
-        if (!w_pub) {  // row bid's routing weights, written before the permutation
-          w_pub = true;
-          __threadfence();
-          atomicAdd(a.sync + kSyncUnits, 1);
-        }
       }
       if (ok) ok = P.issue(J_END, 0, 0, 0);
-      if (!w_pub) {
-        w_pub = true;
-        __threadfence();
-        atomicAdd(a.sync + kSyncUnits, 1);
-      }
       // every unit published
       if (ok) {
         const long long t0 = cycles_now();
@@ -705,11 +691,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
         mbar_wait_bounded(full0 + 8 * (jj % a.nst), (jj / a.nst) & 1, a.status);
     }
     __syncwarp();
+  } else if (warp == kHelperWarp) {
+    // ================= helper: routing weights of row bid =================
+    // float64 softmax over the k selected logits in rank order, one rounding
+    // to fp32; published like a unit (the reduction waits for T of them)
+    if (layer_mode && bid < T) {
+      const int t = bid;
+      const float v = lane < k ? s_topv[t][lane] : 0.f;
+      const double m0 = (double)__shfl_sync(0xffffffffu, v, 0);
+      const double ej = lane < k ? exp((double)v - m0) : 0.0;
+      double sum = 0.0;
+      for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ej, j);
+      if (lane < k) {
+        a.ids_out[(size_t)t * k + lane] = s_ids[t][lane];
+        a.w_out[(size_t)t * k + lane] = (float)(ej / sum);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        atomicAdd(a.sync + kSyncUnits, 1);
+      }
+    }
   } else {
     // ================= consumers =================
     const int cw = warp - 1, mw = cw & 3, kh = cw >> 2, ct = tid - 32;
     const int g = lane >> 2, c = lane & 3;
-    float* const rw = red + mw * (MT * 2 * 4 * 32);  // this row warp's exchange area
+    float* const rw = red + mw * (MT * MAXNT * 4 * 32);  // this row warp's exchange area
+    const uint32_t sw = stg_s + cw * (a.TB * kStgRow * 4);  // this warp's partial staging rows
+    bool bulk_out = false;  // this lane has bulk copies in flight
+    int pub_bar = -1;       // publish barrier of a unit whose partial copies may be in flight
+    // A unit is published once its partial copies are complete (checked one
+    // job later, when they have long landed): every consumer lane arrives.
+    auto publish = [&]() {
+      if (pub_bar < 0) return;
+      if (bulk_out) {
+        bulk_wait_all();
+        fence_proxy_async_global();
+        bulk_out = false;
+      }
+      mbar_arrive(pub0 + 8 * pub_bar);
+      pub_bar = -1;
+    };
     constexpr int HB = UI * 2 + 16;
     float acc[MT][2][4];
     float accd[kDnM][2][4];
@@ -730,7 +752,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
         break;
       }
       const int4 hd = s_hdr[slot];
-      if (hd.x == J_END) break;
+      if (hd.x == J_END) {
+        publish();
+        break;
+      }
       const int kind = hd.x, d = hd.y, grp = hd.z, chunk = hd.w;
       const uint32_t st = sbase + slot * a.stage_bytes;
       uint8_t* hb = hbuf + (ucnt & 1) * (kMaxT * HB);
@@ -758,6 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
         else job_compute<true, MT, MAXNT>(st, mw, kh, a.TB, browx, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * slot);  // this warp is done with the stage
+        publish();
         if (chunk != nch - 1) continue;
 
         // ---- gate/up epilogue: half 1 hands its sums to half 0 (fixed order
@@ -766,21 +792,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
 #pragma unroll
           for (int m = 0; m < MT; ++m)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < MAXNT; ++nt)
               if (nt < ntiles)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) rw[((m * 2 + nt) * 4 + q) * 32 + lane] = acc[m][nt][q];
+                for (int q = 0; q < 4; ++q) rw[((m * MAXNT + nt) * 4 + q) * 32 + lane] = acc[m][nt][q];
         }
         named_bar_sync(1 + mw, 64);
         if (kh == 0) {
 #pragma unroll
           for (int m = 0; m < MT; ++m)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
+            for (int nt = 0; nt < MAXNT; ++nt) {
               if (nt >= ntiles) continue;
               float v[4];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) v[q] = acc[m][nt][q] + rw[((m * 2 + nt) * 4 + q) * 32 + lane];
+              for (int q = 0; q < 4; ++q) v[q] = acc[m][nt][q] + rw[((m * MAXNT + nt) * 4 + q) * 32 + lane];
               // v = (g, g, u, u) of unit row il for token slots 2c, 2c+1
               const int il = 8 * (mw * MT + m) + g;
               const int col = (il & ~7) + perm8_pos(il & 7);
@@ -810,32 +836,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
       else dn_compute<MT, MAXNT>(st, hbs, cw, boff, browh, accd);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+      publish();
       {
-        const bool good = !*abort_flag;
-        const int base = s_act_off[d];
-        const int Gm = a.Gmax;
+        // this warp's 64 output rows for the tokens < cnt: staged as [n][kStgRow]
+        // f32, then one 256-byte bulk copy per token to the partial buffer
+        if (bulk_out) {  // the previous job's copies have read the staging rows
+          bulk_wait_read_all();
+          bulk_out = false;
+        }
+        __syncwarp();
 #pragma unroll
         for (int m = 0; m < kDnM; ++m)
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
+          for (int nt = 0; nt < MAXNT; ++nt) {
             if (nt >= ntiles) continue;
-            const int r = chunk * kDnRows + 16 * (kDnM * cw + m) + g;
 #pragma unroll
             for (int e2 = 0; e2 < 2; ++e2) {
               const int n = nt * 8 + 2 * c + e2;
-              if (good && n < cnt) {
-                float* pp = a.partial + ((size_t)(base + n) * Gm + grp) * H + r;
-                pp[0] = accd[m][nt][e2];
-                pp[8] = accd[m][nt][2 + e2];
+              if (n < cnt) {
+                const uint32_t o = sw + (uint32_t)(n * kStgRow + 16 * m + g) * 4u;
+                st_s_f32(o, accd[m][nt][e2]);
+                st_s_f32(o + 32, accd[m][nt][2 + e2]);
               }
             }
           }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane < cnt && !*abort_flag) {
+          float* dst = a.partial + ((size_t)(s_act_off[d] + lane) * a.Gmax + grp) * H + chunk * kDnRows + 64 * cw;
+          bulk_s2g(dst, sw + (uint32_t)(lane * kStgRow) * 4u, 256);
+          bulk_commit();
+          bulk_out = true;
+        }
       }
       if (chunk == nchd - 1) {
-        mbar_arrive(pub0 + 8 * (ucnt % kPubBars));  // every lane: its partial stores are done
+        pub_bar = ucnt % kPubBars;
         ++ucnt;
       }
     }
+
+    if (bulk_out) bulk_wait_all();
 
     // ---- reduction, once every unit of the window is published. Lane q of an
     // 8-lane group sums, for one output float4,
@@ -853,6 +893,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
           const int t = live ? o / H4 : 0, col = live ? (o - t * H4) * 4 : 0;
           float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
           if (live) {
+            // the first shared-expert slice of this lane, in flight with the routed loads
+            const float* psh = a.partial + (size_t)(Pres + t) * gstride + col;
+            const float4 u0 = has_shared && q < sc.nGs ? ldg_cg_f4(psh + (size_t)q * H) : make_float4(0.f, 0.f, 0.f, 0.f);
             for (int jj = q; jj < k; jj += 8) {
               const int e = s_ids[t][jj];
               const int dd = s_d_of_e[e];
@@ -874,10 +917,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
               v.x = fmaf(wv, sacc.x, v.x); v.y = fmaf(wv, sacc.y, v.y);
               v.z = fmaf(wv, sacc.z, v.z); v.w = fmaf(wv, sacc.w, v.w);
             }
-            if (has_shared) {
-              const float* pp = a.partial + (size_t)(Pres + t) * gstride + col;
-              for (int gg = q; gg < sc.nGs; gg += 8) {
-                const float4 u4 = ldg_cg_f4(pp + (size_t)gg * H);
+            if (has_shared && q < sc.nGs) {
+              v.x += u0.x; v.y += u0.y; v.z += u0.z; v.w += u0.w;
+              for (int gg = q + 8; gg < sc.nGs; gg += 8) {
+                const float4 u4 = ldg_cg_f4(psh + (size_t)gg * H);
                 v.x += u4.x; v.y += u4.y; v.z += u4.z; v.w += u4.w;
               }
             }
@@ -1083,7 +1126,9 @@ static int stages_for(int TB) {
   }
   const int stage = fused::stage_bytes_for(MT, TB);
   int n = fused::kMaxNst;
-  while (n >= 2 && fused::smem_bytes(MT, n, stage) + st > (size_t)optin) --n;
+  while (n >= 2 && fused::smem_bytes(MT, NTX, n, stage, TB) + st > (size_t)optin) --n;
+  // the routing's scratch and the slot map's copy live in the stages
+  if ((size_t)n * stage < (size_t)fused::kSlotMapOff + 4 * kMaxE) return 0;
   return n >= 2 ? n : 0;
 }
 
@@ -1103,7 +1148,7 @@ static cudaError_t launch_mt(fused::Args& a, cudaStream_t st) {
   a.stage_bytes = fused::stage_bytes_for(MT, a.TB);
   a.nst = stages_for<MT, NTX>(a.TB);
   if (a.nst < 2) return cudaErrorInvalidValue;
-  const size_t smem = fused::smem_bytes(MT, a.nst, a.stage_bytes);
+  const size_t smem = fused::smem_bytes(MT, NTX, a.nst, a.stage_bytes, a.TB);
   static std::mutex mu;
   static size_t configured = 0;
   {
