@@ -57,13 +57,20 @@ constexpr int kDnM = kDnRows / (kCW * 16);  // m16 tiles per warp in a down job
 constexpr int kPubCount = kCW * 32;     // arrivals that publish a unit (every consumer lane)
 constexpr int kPubBars = 4;             // publish barriers, used by units in turn
 constexpr int kStgRow = 68;             // floats per token row of a warp's partial staging (64 + 4 pad)
+// Unrolling of the per-block loops of a job (the kernel holds the compute of
+// three unit sizes; full unrolling of all of them crowds the instruction cache).
+constexpr int kBlockUnroll = 4;
+constexpr int kMT = 4;                  // m16 tiles per row warp in a full unit
+constexpr int kUI = 32 * kMT;           // intermediate rows of a full unit (a half unit has 64)
 constexpr uint32_t kBf16NegMagic = 0xC308C308u;  // bf16 -136
 constexpr uint32_t kF16NegMagic = 0xE408E408u;   // f16 -1032
 
 // cross-CTA counters (int32 offsets in the workspace sync region)
 constexpr int kSyncDone = 0, kSyncUnits = 1, kSyncQueue = 2;
 
-enum JobKind : int { J_GU = 0, J_DN = 1, J_END = 2 };
+// Jobs of full units (kUI intermediate rows) and half units (64): gate/up
+// kind 2 s, down kind 2 s + 1 for unit size s = 0 (full), 1 (half).
+enum JobKind : int { J_GU = 0, J_DN = 1, J_GUH = 2, J_DNH = 3, J_END = 4 };
 
 struct Args {
   // TMA tensor maps (kernel parameters, read through their parameter address)
@@ -71,9 +78,13 @@ struct Args {
   CUtensorMap tm_gs, tm_us, tm_ds;     // routed scales
   CUtensorMap tm_sgc, tm_suc, tm_sdc;  // shared expert codes
   CUtensorMap tm_sgs, tm_sus, tm_sds;  // shared expert scales
+  CUtensorMap tm_gch, tm_uch, tm_dch;  // the same in half-unit boxes (64 rows; 32-byte down rows)
+  CUtensorMap tm_gsh, tm_ush;
+  CUtensorMap tm_sgch, tm_such, tm_sdch;
+  CUtensorMap tm_sgsh, tm_sush;
   CUtensorMap tm_x;                    // x [T][H] bf16, 3D box (64, 4, TB)
   int H, I, shI, E, k, S, T;
-  int Gmax;        // slices of I per partial row (max(I, shared I) / UI)
+  int Gh;          // 64-column slices of I per partial row (max(I, shared I) / 64)
   int TB;          // rows of the x / h boxes (8 or 16, >= T)
   int nst;         // stages in the ring
   int stage_bytes; // multiple of 1024
@@ -87,16 +98,20 @@ struct Args {
   float* y;
   int32_t* miss_ids;
   int32_t* n_miss;
-  float* partial;          // [rows_cap][Gmax][H]: one down partial per routed pair and slice
+  // [rows_cap][Gh][H]: the down partials of each routed pair (and shared row):
+  // a full unit's A + B at slice 2 g, a half unit's A or B at its own slice
+  float* partial;
   int32_t* status;
   int32_t* sync;
 };
 
-// Stage layouts (byte offsets from the 1024-aligned stage base), UI = 32 MT:
+// Stage layouts (byte offsets from the 1024-aligned stage base), UI = 32 MT
+// (MT = 4 for full units, 2 for half units):
 //  gate/up: gate codes [UI][128 B] (swizzled), up codes [UI][128 B], x box
 //           [TB][4][128 B] (swizzled), gate scales [UI][8], up scales [UI][8];
-//  down:    codes [512][UI/2 B] (swizzled for UI/2 = 64 or 32 bytes), scales
-//           [512][8] (the 8 blocks around the unit's UI columns).
+//  down:    codes [512][UI/2 B] (swizzled by the row width, 64 or 32 bytes),
+//           scales [512][8] (the 8 blocks
+//           around the unit's UI columns).
 __host__ __device__ constexpr int gu_job_bytes(int MT, int TB) { return 288 * 32 * MT + 512 * TB; }
 __host__ __device__ constexpr int dn_job_bytes(int MT) { return kDnRows * 16 * MT + 16 * kDnRows; }
 __host__ __device__ constexpr int stage_bytes_for(int MT, int TB) {
@@ -247,7 +262,7 @@ __device__ __forceinline__ void job_compute(uint32_t st, int mw, int kh, int TB,
   const uint32_t rowp = st + r0 * 128 + c * 4;
   const uint32_t sclp = scl0 + r0 * 16;
   constexpr int kMStep = GU ? 8 : 16;  // rows between m-tiles
-#pragma unroll
+#pragma unroll kBlockUnroll
   for (int i = 0; i < 4; ++i) {
     const int b = kh * 4 + i;
     uint4 braw[NT];
@@ -315,6 +330,10 @@ __device__ __forceinline__ void job_compute(uint32_t st, int mw, int kh, int TB,
   }
 }
 
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
 __device__ __forceinline__ float4 ldg_cg_f4(const float* p) {
   const uint4 v = ldg_cg_v4(p);
   return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
@@ -327,7 +346,8 @@ __device__ __forceinline__ float4 ldg_cg_f4(const float* p) {
 // Codes: [512][UI/2 B] with the TMA swizzle of that row width (64-, 32-byte or
 // none); scales [512][8] (the unit's blocks start at boff); h comes from the
 // unit's shared-memory buffer [slot][UI + 8] f16 in fragment order.
-template <int MT, int NT>
+// Blocks B0 .. B0 + NB - 1 of the unit's MT, summed in block order.
+template <int MT, int NT, int B0, int NB>
 __device__ __forceinline__ void dn_compute(uint32_t st, uint32_t hb, int cw, int boff,
                                            const int (&brow)[2], float (&acc)[kDnM][2][4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
@@ -335,8 +355,8 @@ __device__ __forceinline__ void dn_compute(uint32_t st, uint32_t hb, int cw, int
   constexpr uint32_t kSwz = MT == 4 ? 3u : (MT == 2 ? 1u : 0u);
   constexpr int HB = UI * 2 + 16;
   const uint32_t scl = st + kDnRows * RB;
-#pragma unroll
-  for (int b = 0; b < MT; ++b) {
+#pragma unroll kBlockUnroll
+  for (int b = B0; b < B0 + NB; ++b) {
     uint32_t bf[NT][4];
     float corr[NT][4];
 #pragma unroll
@@ -378,25 +398,59 @@ __device__ __forceinline__ void dn_compute(uint32_t st, uint32_t hb, int cw, int
   }
 }
 
-// The units of a window, in queue order: the shared expert's, then the routed
-// experts' (expert order). Unit (d, g) is intermediate rows [g UI, g UI + UI)
-// of expert d: its gate/up (H / 256 jobs) and that slice's share of the down
-// projection (H / 256 jobs of 256 output rows).
+// The units of a window, in queue order. Group (d, g) is intermediate rows
+// [g kUI, g kUI + kUI) of expert d, groups in the order: the shared expert's,
+// then the routed experts' (expert order). The first nfull groups are full
+// units; each later group is split into sf units of 128 / sf rows. A unit is
+// its gate/up (H / 256 jobs) and its rows' share of the down projection
+// (H / 512 jobs of 512 output rows).
+//
+// nfull balances the window over the G CTAs. Unsplit, U groups take M0 =
+// ceil(U / G) rounds of full units. Splitting the R groups of the last round
+// into halves instead takes M0 - 1 rounds plus ceil(2 R / G) rounds of half
+// units, each costing about kHalfCostPct % of a full unit (measured: the fixed
+// costs of a unit do not halve with its bytes); the cheaper plan is taken. The
+// dynamic queue hands out the full units first, so the halves fill the CTAs
+// that finish first. The results do not depend on the split: a group's down
+// partial is A + B, A and B the scaled sums (fma chains) of its blocks 0-1 and
+// 2-3, formed by one full unit or by its two halves, and added in the reduction.
+constexpr int kHalfCostPct = 68;
 struct Sched {
   int D;      // resident routed experts of the window (the shared expert is d = D)
-  int nGs;    // units of the shared expert (0 without one)
-  int nGi;    // units per routed expert
+  int nGs;    // groups of the shared expert (0 without one)
+  int nGi;    // groups per routed expert
+  int U;      // groups in all
+  int nfull;  // groups that stay whole (the first nfull in queue order)
   int total;  // units in all
-  __device__ int2 unit(int t) const {  // (d, g)
-    if (t < nGs) return make_int2(D, t);
-    const int d = (t - nGs) / nGi;
-    return make_int2(d, t - nGs - d * nGi);
+  __device__ void plan(int G) {
+    U = nGs + D * nGi;
+    const int M0 = (U + G - 1) / G;
+    const int R = U - G * (M0 - 1);
+    const int ch = 100 * (M0 - 1) + kHalfCostPct * ((2 * R + G - 1) / G);
+    nfull = (U > 0 && ch < 100 * M0) ? U - R : U;
+    total = nfull + 2 * (U - nfull);
   }
+  __device__ int2 group(int u) const {  // (d, g) of group u
+    if (u < nGs) return make_int2(D, u);
+    const int d = (u - nGs) / nGi;
+    return make_int2(d, u - nGs - d * nGi);
+  }
+  // unit t -> (d, its first 32-row slice of I: 4 g or 4 g + 2, size: 0 full, 1 half)
+  __device__ int3 unit(int t) const {
+    if (t < nfull) {
+      const int2 dg = group(t);
+      return make_int3(dg.x, 4 * dg.y, 0);
+    }
+    const int x = t - nfull;
+    const int2 dg = group(nfull + (x >> 1));
+    return make_int3(dg.x, 4 * dg.y + 2 * (x & 1), 1);
+  }
+  // group index of (d, g): d = D is the shared expert
+  __device__ int group_index(int d, int g) const { return d == D ? g : nGs + d * nGi + g; }
 };
 
 // The producer thread's state and steps (always inlined: no call may make it
 // wait for an atomic whose result it does not need yet).
-template <int MT>
 struct Producer {
   const Args& a;
   uint32_t sbase, full0, empty0, pub0;
@@ -439,11 +493,11 @@ struct Producer {
   __device__ __forceinline__ void wait_pub(uint32_t ns) {
     if (pd < ui) mbar_try_wait_ns(pub0 + 8 * (pd % kPubBars), (pd / kPubBars) & 1, ns);
   }
-  __device__ __forceinline__ bool issue(int kind, int d, int grp, int chunk) {
-    constexpr int UI = 32 * MT;
+  // qi: the unit's first 32-row slice of the expert's I (4 g for a full unit)
+  __device__ __forceinline__ bool issue(int kind, int d, int qi, int chunk) {
     if ((j & 3) == 0) poll();  // publications are also handled whenever the producer waits
     if (!acquire_slot()) return false;
-    hdr[slot] = make_int4(kind, d, grp, chunk);
+    hdr[slot] = make_int4(kind, d, qi, chunk);
     const uint32_t st = sbase + slot * stage_bytes, fb = full0 + 8 * slot;
     ++j;
     if (++slot == nst) {
@@ -456,25 +510,33 @@ struct Producer {
     }
     const bool sh = d == D;
     const int slotp = sh ? 0 : act_slot[d];
-    if (kind == J_GU) {
-      mbar_expect_tx(fb, (uint32_t)gu_job_bytes(MT, a.TB));
-      const int row = (sh ? 0 : slotp * a.I) + grp * UI;
-      tma_load_2d_hint(st, sh ? &a.tm_sgc : &a.tm_gc, chunk * 128, row, fb, wpol);
-      tma_load_2d_hint(st + UI * 128, sh ? &a.tm_suc : &a.tm_uc, chunk * 128, row, fb, wpol);
-      tma_load_3d(st + 2 * UI * 128, &a.tm_x, 0, chunk * 4, 0, fb);
+    if ((kind & 1) == 0) {  // gate/up of a unit of size s: UI = kUI >> s rows
+      const int sz = kind >> 1, UI = kUI >> sz;
+      mbar_expect_tx(fb, (uint32_t)gu_job_bytes(kMT >> sz, a.TB));
+      const int row = (sh ? 0 : slotp * a.I) + qi * 32;
       const uint32_t so = st + 2 * UI * 128 + a.TB * 512;
-      tma_load_2d_hint(so, sh ? &a.tm_sgs : &a.tm_gs, chunk * 8, row, fb, wpol);
-      tma_load_2d_hint(so + UI * 16, sh ? &a.tm_sus : &a.tm_us, chunk * 8, row, fb, wpol);
-    } else {
-      mbar_expect_tx(fb, (uint32_t)dn_job_bytes(MT));
+      const bool hf = sz == 1;
+      tma_load_2d_hint(st, hf ? (sh ? &a.tm_sgch : &a.tm_gch) : (sh ? &a.tm_sgc : &a.tm_gc), chunk * 128,
+                       row, fb, wpol);
+      tma_load_2d_hint(st + UI * 128, hf ? (sh ? &a.tm_such : &a.tm_uch) : (sh ? &a.tm_suc : &a.tm_uc),
+                       chunk * 128, row, fb, wpol);
+      tma_load_2d_hint(so, hf ? (sh ? &a.tm_sgsh : &a.tm_gsh) : (sh ? &a.tm_sgs : &a.tm_gs), chunk * 8,
+                       row, fb, wpol);
+      tma_load_2d_hint(so + UI * 16, hf ? (sh ? &a.tm_sush : &a.tm_ush) : (sh ? &a.tm_sus : &a.tm_us),
+                       chunk * 8, row, fb, wpol);
+      tma_load_3d(st + 2 * UI * 128, &a.tm_x, 0, chunk * 4, 0, fb);
+    } else {  // down: the unit's columns of 512 rows
+      const int sz = kind >> 1;
+      const int RB = (kUI / 2) >> sz;  // code bytes of a down row in the unit's columns
+      mbar_expect_tx(fb, (uint32_t)dn_job_bytes(kMT >> sz));
       const int row = (sh ? 0 : slotp * a.H) + chunk * kDnRows;
-      const uint32_t so = st + kDnRows * (UI / 2);
+      const uint32_t so = st + kDnRows * RB;
+      const CUtensorMap* dc = sz == 0 ? (sh ? &a.tm_sdc : &a.tm_dc) : (sh ? &a.tm_sdch : &a.tm_dch);
 #pragma unroll
       for (int h2 = 0; h2 < kDnRows / 256; ++h2) {  // boxes of 256 rows
-        tma_load_2d_hint(st + h2 * 256 * (UI / 2), sh ? &a.tm_sdc : &a.tm_dc, grp * (UI / 2),
-                         row + 256 * h2, fb, wpol);
-        tma_load_2d_hint(so + h2 * 256 * 16, sh ? &a.tm_sds : &a.tm_ds, (grp * MT) & ~7,
-                         row + 256 * h2, fb, wpol);
+        tma_load_2d_hint(st + h2 * 256 * RB, dc, qi * 16, row + 256 * h2, fb, wpol);
+        tma_load_2d_hint(so + h2 * 256 * 16, sh ? &a.tm_sds : &a.tm_ds, qi & ~7, row + 256 * h2,
+                         fb, wpol);
       }
     }
     return true;
@@ -482,7 +544,7 @@ struct Producer {
 };
 
 // MAXNT: n8 token tiles at most (1 for windows of up to 8 rows, 2 beyond).
-template <int MT, int MAXNT>
+template <int MAXNT>
 __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_constant__ Args a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ int s_ids[kMaxT][kMaxK];
@@ -498,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   __shared__ uint32_t s_total;
   __shared__ int s_abort;
 
-  constexpr int UI = 32 * MT;
+  constexpr int MT = kMT, UI = kUI;  // full units; half units have MT = 2
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, bid = blockIdx.x;
   const int T = a.T, k = a.k, E = a.E, H = a.H;
@@ -525,10 +587,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     for (int i = 0; i < kPubBars; ++i) mbar_init(pub0 + 8 * i, kPubCount);
     fence_barrier_init();
     // the tensor maps' descriptors (kernel parameters), fetched ahead of use
-    const CUtensorMap* maps[] = {&a.tm_gc, &a.tm_uc, &a.tm_dc, &a.tm_gs, &a.tm_us, &a.tm_ds, &a.tm_x};
+    const CUtensorMap* maps[] = {&a.tm_gc, &a.tm_uc, &a.tm_dc, &a.tm_gs, &a.tm_us, &a.tm_ds, &a.tm_x,
+                                 &a.tm_gch, &a.tm_uch, &a.tm_dch, &a.tm_gsh, &a.tm_ush};
     for (const CUtensorMap* m : maps) prefetch_tensormap(m);
     if (has_shared) {
-      const CUtensorMap* smaps[] = {&a.tm_sgc, &a.tm_suc, &a.tm_sdc, &a.tm_sgs, &a.tm_sus, &a.tm_sds};
+      const CUtensorMap* smaps[] = {&a.tm_sgc, &a.tm_suc, &a.tm_sdc, &a.tm_sgs, &a.tm_sus, &a.tm_sds,
+                                    &a.tm_sgch, &a.tm_such, &a.tm_sdch, &a.tm_sgsh, &a.tm_sush};
       for (const CUtensorMap* m : smaps) prefetch_tensormap(m);
     }
     // the next kernel of the stream may be scheduled now: it takes an SM only
@@ -643,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   const int Pres = (tot >> 22) & 0x3ff;
   sc.nGs = has_shared ? a.shI / UI : 0;
   sc.nGi = a.I / UI;
-  sc.total = sc.nGs + sc.D * sc.nGi;
+  sc.plan(G);
   const int D = sc.D;
   const int nch = H / kKC;        // gate/up jobs (256 columns) per unit
   const int nchd = H / kDnRows;   // down jobs (512 rows) per unit
@@ -654,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     if (lane == 0) {
       // ================= producer (one thread) =================
       fence_proxy_async_shared();  // the top-k scratch in stage memory precedes the TMA writes
-      Producer<MT> P{a, sbase, full0, empty0, pub0, s_hdr, s_act_slot, D, a.nst, a.stage_bytes,
+      Producer P{a, sbase, full0, empty0, pub0, s_hdr, s_act_slot, D, a.nst, a.stage_bytes,
                      l2_evict_first_policy(), 0, 0, 0, 0, 0};
       bool ok = true;
       int next = ticket;
@@ -668,11 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
           }
           if (!ok) break;
         }
-        const int2 u = sc.unit(ticket);
+        const int3 u = sc.unit(ticket);
         ++P.ui;
         next = atomicAdd(a.sync + kSyncQueue, 1);  // needed at the next unit only
-        for (int ch = 0; ch < nch && ok; ++ch) ok = P.issue(J_GU, u.x, u.y, ch);
-        for (int ch = 0; ch < nchd && ok; ++ch) ok = P.issue(J_DN, u.x, u.y, ch);
+        for (int ch = 0; ch < nch && ok; ++ch) ok = P.issue(2 * u.z, u.x, u.y, ch);
+        for (int ch = 0; ch < nchd && ok; ++ch) ok = P.issue(2 * u.z + 1, u.x, u.y, ch);
         ticket = next;
       }
       if (ok) ok = P.issue(J_END, 0, 0, 0);
@@ -718,21 +782,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     const int g = lane >> 2, c = lane & 3;
     float* const rw = red + mw * (MT * MAXNT * 4 * 32);  // this row warp's exchange area
     const uint32_t sw = stg_s + cw * (a.TB * kStgRow * 4);  // this warp's partial staging rows
-    bool bulk_out = false;  // this lane has bulk copies in flight
+    bool bulk_rd = false;   // this lane's bulk copies may still read its staging rows
+    bool bulk_wr = false;   // ... or still be writing the partial buffer
     int pub_bar = -1;       // publish barrier of a unit whose partial copies may be in flight
     // A unit is published once its partial copies are complete (checked one
     // job later, when they have long landed): every consumer lane arrives.
     auto publish = [&]() {
       if (pub_bar < 0) return;
-      if (bulk_out) {
+      if (bulk_wr) {
         bulk_wait_all();
         fence_proxy_async_global();
-        bulk_out = false;
+        bulk_wr = bulk_rd = false;
       }
       mbar_arrive(pub0 + 8 * pub_bar);
       pub_bar = -1;
     };
-    constexpr int HB = UI * 2 + 16;
     float acc[MT][2][4];
     float accd[kDnM][2][4];
     int browx[2] = {0, 0};  // x box row (token) of token slot nt*8 + g
@@ -756,11 +820,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
         publish();
         break;
       }
-      const int kind = hd.x, d = hd.y, grp = hd.z, chunk = hd.w;
+      const int kind = hd.x, d = hd.y, qi = hd.z, chunk = hd.w;
+      const int sz = kind >> 1;               // 0 full, 1 half unit
+      const int mta = MT >> sz;               // m16 tiles per row warp in this unit
+      const int HB = 64 * mta + 16;           // bytes per token row of the h buffer
       const uint32_t st = sbase + slot * a.stage_bytes;
-      uint8_t* hb = hbuf + (ucnt & 1) * (kMaxT * HB);
+      uint8_t* hb = hbuf + (ucnt & 1) * (hb_bytes(MT) / 2);
       const uint32_t hbs = smem_u32(hb);
-      if (kind == J_GU) {
+      if ((kind & 1) == 0) {
         if (chunk == 0) {
 #pragma unroll
           for (int m = 0; m < MT; ++m)
@@ -779,8 +846,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
             browx[nt] = sh ? nb : nth_bit(mask, nb);
           }
         }
-        if (MAXNT == 1 || ntiles == 1) job_compute<true, MT, 1>(st, mw, kh, a.TB, browx, acc);
-        else job_compute<true, MT, MAXNT>(st, mw, kh, a.TB, browx, acc);
+        float(&acc2)[2][2][4] = *reinterpret_cast<float(*)[2][2][4]>(&acc[0]);
+        if (sz == 1) {
+          if (MAXNT == 1 || ntiles == 1) job_compute<true, 2, 1>(st, mw, kh, a.TB, browx, acc2);
+          else job_compute<true, 2, MAXNT>(st, mw, kh, a.TB, browx, acc2);
+        } else {
+          if (MAXNT == 1 || ntiles == 1) job_compute<true, MT, 1>(st, mw, kh, a.TB, browx, acc);
+          else job_compute<true, MT, MAXNT>(st, mw, kh, a.TB, browx, acc);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * slot);  // this warp is done with the stage
         publish();
@@ -793,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
           for (int m = 0; m < MT; ++m)
 #pragma unroll
             for (int nt = 0; nt < MAXNT; ++nt)
-              if (nt < ntiles)
+              if (m < mta && nt < ntiles)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) rw[((m * MAXNT + nt) * 4 + q) * 32 + lane] = acc[m][nt][q];
         }
@@ -803,12 +876,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
           for (int m = 0; m < MT; ++m)
 #pragma unroll
             for (int nt = 0; nt < MAXNT; ++nt) {
-              if (nt >= ntiles) continue;
+              if (m >= mta || nt >= ntiles) continue;
               float v[4];
 #pragma unroll
               for (int q = 0; q < 4; ++q) v[q] = acc[m][nt][q] + rw[((m * MAXNT + nt) * 4 + q) * 32 + lane];
               // v = (g, g, u, u) of unit row il for token slots 2c, 2c+1
-              const int il = 8 * (mw * MT + m) + g;
+              const int il = 8 * (mw * mta + m) + g;
               const int col = (il & ~7) + perm8_pos(il & 7);
 #pragma unroll
               for (int e2 = 0; e2 < 2; ++e2) {
@@ -824,25 +897,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
         continue;
       }
 
-      // ---- down job: 256 output rows of this unit's slice of I
+      // ---- down job: 512 output rows of this unit's columns of I. This warp's
+      // 64 rows for the tokens < cnt are staged as [n][kStgRow] f32, then go
+      // to the partial buffer by one 256-byte bulk copy per token. A full unit
+      // sums A (blocks 0-1) and B (blocks 2-3) separately and stages A + B.
+      auto zero_acc = [&]() {
 #pragma unroll
-      for (int m = 0; m < kDnM; ++m)
+        for (int m = 0; m < kDnM; ++m)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+          for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) accd[m][nt][q] = 0.f;
-      const int boff = (grp * MT) & 7;
-      if (MAXNT == 1 || ntiles == 1) dn_compute<MT, 1>(st, hbs, cw, boff, browh, accd);
-      else dn_compute<MT, MAXNT>(st, hbs, cw, boff, browh, accd);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-      publish();
-      {
-        // this warp's 64 output rows for the tokens < cnt: staged as [n][kStgRow]
-        // f32, then one 256-byte bulk copy per token to the partial buffer
-        if (bulk_out) {  // the previous job's copies have read the staging rows
+            for (int q = 0; q < 4; ++q) accd[m][nt][q] = 0.f;
+      };
+      auto stage_out = [&]() {
+        if (bulk_rd) {  // the previous job's copies have read the staging rows
           bulk_wait_read_all();
-          bulk_out = false;
+          bulk_rd = false;
         }
         __syncwarp();
 #pragma unroll
@@ -860,13 +930,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
               }
             }
           }
+      };
+      const int boff = qi & 7;
+      const bool nt1 = MAXNT == 1 || ntiles == 1;
+      zero_acc();
+      if (sz == 0) {
+        float accb[kDnM][2][4];
+#pragma unroll
+        for (int m = 0; m < kDnM; ++m)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) accb[m][nt][q] = 0.f;
+        if (nt1) {
+          dn_compute<MT, 1, 0, 2>(st, hbs, cw, boff, browh, accd);
+          dn_compute<MT, 1, 2, 2>(st, hbs, cw, boff, browh, accb);
+        } else {
+          dn_compute<MT, MAXNT, 0, 2>(st, hbs, cw, boff, browh, accd);
+          dn_compute<MT, MAXNT, 2, 2>(st, hbs, cw, boff, browh, accb);
+        }
+#pragma unroll
+        for (int m = 0; m < kDnM; ++m)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) accd[m][nt][q] += accb[m][nt][q];
+      } else {  // half unit: A or B of its group
+        if (nt1) dn_compute<2, 1, 0, 2>(st, hbs, cw, boff, browh, accd);
+        else dn_compute<2, MAXNT, 0, 2>(st, hbs, cw, boff, browh, accd);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+      publish();
+      {
+        stage_out();
         fence_proxy_async_shared();
         __syncwarp();
         if (lane < cnt && !*abort_flag) {
-          float* dst = a.partial + ((size_t)(s_act_off[d] + lane) * a.Gmax + grp) * H + chunk * kDnRows + 64 * cw;
+          float* dst = a.partial + ((size_t)(s_act_off[d] + lane) * a.Gh + (qi >> 1)) * H + chunk * kDnRows + 64 * cw;
           bulk_s2g(dst, sw + (uint32_t)(lane * kStgRow) * 4u, 256);
           bulk_commit();
-          bulk_out = true;
+          bulk_rd = bulk_wr = true;
         }
       }
       if (chunk == nchd - 1) {
@@ -875,27 +979,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
       }
     }
 
-    if (bulk_out) bulk_wait_all();
+    if (bulk_wr) bulk_wait_all();
 
     // ---- reduction, once every unit of the window is published. Lane q of an
     // 8-lane group sums, for one output float4,
-    //   v_q = sum_{j = q, q+8, ..} w_tj sum_g p(e_tj, g)[t] + sum_{g = q, q+8, ..} p(shared, g)[t]
-    // (g in order), and y = v_0 + ... + v_7 in lane order: a fixed order on every CTA.
+    //   v_q = sum_{j = q, q+8, ..} w_tj sum_g n(e_tj, g)[t] + sum_{g = q, q+8, ..} n(shared, g)[t]
+    // (g in order; n the group's down partial, A + B from its halves if it was split),
+    // and y = v_0 + ... + v_7 in lane order: a fixed order on every CTA, for any
+    // window and any split.
     if (!*abort_flag) {
       if (ct == 0 && !wait_counter_bounded(a.sync + kSyncUnits, target, a.status)) *abort_flag = 1;
       named_bar_sync(6, kCW * 32);
       if (!*abort_flag) {
         const int q = ct & 7, H4 = H / 4, NO = T * H4;
-        const size_t gstride = (size_t)a.Gmax * H;
+        const size_t gstride = (size_t)a.Gh * H;
         for (int o0 = bid * (kCW * 4); o0 < NO; o0 += G * (kCW * 4)) {
           const int o = o0 + (ct >> 3);
           const bool live = o < NO;
           const int t = live ? o / H4 : 0, col = live ? (o - t * H4) * 4 : 0;
           float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
           if (live) {
-            // the first shared-expert slice of this lane, in flight with the routed loads
+            // the first shared-expert group of this lane, in flight with the routed loads
             const float* psh = a.partial + (size_t)(Pres + t) * gstride + col;
-            const float4 u0 = has_shared && q < sc.nGs ? ldg_cg_f4(psh + (size_t)q * H) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 u0 = has_shared && q < sc.nGs ? ldg_cg_f4(psh + (size_t)(2 * q) * H) : make_float4(0.f, 0.f, 0.f, 0.f);
             for (int jj = q; jj < k; jj += 8) {
               const int e = s_ids[t][jj];
               const int dd = s_d_of_e[e];
@@ -904,11 +1010,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
               const float wv = layer_mode ? ldg_cg_f32(a.w_out + (size_t)t * k + jj) : a.w_in[(size_t)t * k + jj];
               const float* pp = a.partial + (size_t)pos * gstride + col;
               float4 sacc = make_float4(0.f, 0.f, 0.f, 0.f);
-              for (int g0 = 0; g0 < sc.nGi; g0 += 8) {  // 8 slices' loads in flight
+              for (int g0 = 0; g0 < sc.nGi; g0 += 8) {  // 8 groups' loads in flight
                 float4 pv[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                  pv[u] = g0 + u < sc.nGi ? ldg_cg_f4(pp + (size_t)(g0 + u) * H) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  pv[u] = g0 + u < sc.nGi ? ldg_cg_f4(pp + (size_t)(2 * (g0 + u)) * H) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                  if (g0 + u < sc.nGi && sc.group_index(dd, g0 + u) >= sc.nfull)
+                    pv[u] = add4(pv[u], ldg_cg_f4(pp + (size_t)(2 * (g0 + u) + 1) * H));
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                   sacc.x += pv[u].x; sacc.y += pv[u].y; sacc.z += pv[u].z; sacc.w += pv[u].w;
@@ -918,9 +1028,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
               v.z = fmaf(wv, sacc.z, v.z); v.w = fmaf(wv, sacc.w, v.w);
             }
             if (has_shared && q < sc.nGs) {
-              v.x += u0.x; v.y += u0.y; v.z += u0.z; v.w += u0.w;
-              for (int gg = q + 8; gg < sc.nGs; gg += 8) {
-                const float4 u4 = ldg_cg_f4(psh + (size_t)gg * H);
+              for (int gg = q; gg < sc.nGs; gg += 8) {
+                float4 u4 = gg == q ? u0 : ldg_cg_f4(psh + (size_t)(2 * gg) * H);
+                if (sc.group_index(D, gg) >= sc.nfull) u4 = add4(u4, ldg_cg_f4(psh + (size_t)(2 * gg + 1) * H));
                 v.x += u4.x; v.y += u4.y; v.z += u4.z; v.w += u4.w;
               }
             }
@@ -1069,31 +1179,14 @@ bool act_map(CUtensorMap* m, const void* p, int cols, int rows, int box_rows) {
 
 static int box_rows(int T) { return T <= 8 ? 8 : 16; }
 
-// Rows per unit: UI = 32 MT intermediate rows. The largest MT that still gives
-// every SM a unit, by the expected number of distinct experts of T rows routed
-// uniformly (skewed routing touches fewer). MT decides which rows a warp owns
-// and how I is cut into slices for the down partials.
-int fused_choose_mt(int E, int k, int T, int I, int shI) {
-  const double p = 1.0 - (double)k / (double)E;
-  double pt = 1.0;
-  for (int t = 0; t < T; ++t) pt *= p;
-  const double d_est = (double)E * (1.0 - pt);
-  const int G = num_sms();
-  for (int mt = 4; mt > 1; mt /= 2) {
-    const int ui = 32 * mt;
-    if (I % ui || (shI % ui)) continue;
-    const double units = d_est * (I / ui) + shI / ui;
-    if (units >= G) return mt;
-  }
-  return 1;
-}
-
+// Slices of I per partial row of the one-launch path: one per 64 intermediate
+// columns (a full unit writes every second, a half unit its own).
 int fused_partial_slices(int E, int k, int T, int I, int shI) {
-  const int mt = fused_choose_mt(E, k, T, I, shI);
-  return (I > shI ? I : shI) / (32 * mt);
+  (void)E; (void)k; (void)T;
+  return (I > shI ? I : shI) / 64;
 }
 
-template <int MT, int NTX>
+template <int NTX>
 static cudaError_t kernel_attrs(size_t* static_smem, int* optin) {
   static std::mutex mu;
   static size_t st = 0;
@@ -1101,7 +1194,7 @@ static cudaError_t kernel_attrs(size_t* static_smem, int* optin) {
   std::lock_guard<std::mutex> lk(mu);
   if (opt == 0) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, fused::decode_layer_kernel<MT, NTX>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, fused::decode_layer_kernel<NTX>);
     if (e != cudaSuccess) return e;
     int dev = 0, o = 0;
     e = cudaGetDevice(&dev);
@@ -1116,11 +1209,12 @@ static cudaError_t kernel_attrs(size_t* static_smem, int* optin) {
 }
 
 // Stages that fit next to the kernel's static shared memory (0: not even two).
-template <int MT, int NTX>
+template <int NTX>
 static int stages_for(int TB) {
+  constexpr int MT = fused::kMT;
   size_t st = 0;
   int optin = 0;
-  if (kernel_attrs<MT, NTX>(&st, &optin) != cudaSuccess) {
+  if (kernel_attrs<NTX>(&st, &optin) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1138,15 +1232,14 @@ bool fused_decode_supported(int H, int I, int shI, int T, bool x_bf16) {
   if (H > 8192 || T > num_sms()) return false;
   if (!encode_fn()) return false;
   const int TB = box_rows(T);
-  if (TB == 8)
-    return stages_for<4, 1>(TB) >= 2 && stages_for<2, 1>(TB) >= 2 && stages_for<1, 1>(TB) >= 2;
-  return stages_for<4, 2>(TB) >= 2 && stages_for<2, 2>(TB) >= 2 && stages_for<1, 2>(TB) >= 2;
+  return TB == 8 ? stages_for<1>(TB) >= 2 : stages_for<2>(TB) >= 2;
 }
 
-template <int MT, int NTX>
-static cudaError_t launch_mt(fused::Args& a, cudaStream_t st) {
+template <int NTX>
+static cudaError_t launch_nt(fused::Args& a, cudaStream_t st) {
+  constexpr int MT = fused::kMT;
   a.stage_bytes = fused::stage_bytes_for(MT, a.TB);
-  a.nst = stages_for<MT, NTX>(a.TB);
+  a.nst = stages_for<NTX>(a.TB);
   if (a.nst < 2) return cudaErrorInvalidValue;
   const size_t smem = fused::smem_bytes(MT, NTX, a.nst, a.stage_bytes, a.TB);
   static std::mutex mu;
@@ -1154,7 +1247,7 @@ static cudaError_t launch_mt(fused::Args& a, cudaStream_t st) {
   {
     std::lock_guard<std::mutex> lk(mu);
     if (smem > configured) {
-      cudaError_t e = cudaFuncSetAttribute(fused::decode_layer_kernel<MT, NTX>,
+      cudaError_t e = cudaFuncSetAttribute(fused::decode_layer_kernel<NTX>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) {
         cudaGetLastError();
@@ -1176,19 +1269,18 @@ static cudaError_t launch_mt(fused::Args& a, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   launch_begin(K_FUSED, st);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, fused::decode_layer_kernel<MT, NTX>, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, fused::decode_layer_kernel<NTX>, a);
   launch_end(st);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st) {
   const int TB = box_rows(f.T);
-  const int MT = fused_choose_mt(f.E, f.k, f.T, f.I, f.shI);
-  const int UI = 32 * MT, DR = 256;  // down boxes of 256 rows
+  const int UI = fused::kUI, HI = fused::kUI / 2, DR = 256;  // down boxes of 256 rows
   fused::Args a;
   std::memset(&a, 0, sizeof a);
   a.H = f.H; a.I = f.I; a.shI = f.shI; a.E = f.E; a.k = f.k; a.S = f.S; a.T = f.T;
-  a.Gmax = (f.I > f.shI ? f.I : f.shI) / UI;
+  a.Gh = fused_partial_slices(f.E, f.k, f.T, f.I, f.shI);
   a.TB = TB;
   a.rows_cap = f.rows_cap;
   const int H = f.H, I = f.I, S = f.S;
@@ -1198,6 +1290,11 @@ cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st) {
             scales_map(&a.tm_gs, f.gs, H, S * I, UI) &&
             scales_map(&a.tm_us, f.us, H, S * I, UI) &&
             scales_map(&a.tm_ds, f.ds, I, S * H, DR) &&
+            codes_map(&a.tm_gch, f.gq, H, S * I, 128, HI) &&
+            codes_map(&a.tm_uch, f.uq, H, S * I, 128, HI) &&
+            codes_map(&a.tm_dch, f.dq, I, S * H, HI / 2, DR) &&
+            scales_map(&a.tm_gsh, f.gs, H, S * I, HI) &&
+            scales_map(&a.tm_ush, f.us, H, S * I, HI) &&
             act_map(&a.tm_x, f.x, H, f.T, TB);
   if (ok && f.shI > 0)
     ok = codes_map(&a.tm_sgc, f.sgq, H, f.shI, 128, UI) &&
@@ -1205,7 +1302,12 @@ cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st) {
          codes_map(&a.tm_sdc, f.sdq, f.shI, H, UI / 2, DR) &&
          scales_map(&a.tm_sgs, f.sgs, H, f.shI, UI) &&
          scales_map(&a.tm_sus, f.sus, H, f.shI, UI) &&
-         scales_map(&a.tm_sds, f.sds, f.shI, H, DR);
+         scales_map(&a.tm_sds, f.sds, f.shI, H, DR) &&
+         codes_map(&a.tm_sgch, f.sgq, H, f.shI, 128, HI) &&
+         codes_map(&a.tm_such, f.suq, H, f.shI, 128, HI) &&
+         codes_map(&a.tm_sdch, f.sdq, f.shI, H, HI / 2, DR) &&
+         scales_map(&a.tm_sgsh, f.sgs, H, f.shI, HI) &&
+         scales_map(&a.tm_sush, f.sus, H, f.shI, HI);
   if (!ok) return cudaErrorInvalidValue;
   a.logits = f.logits; a.ids_in = f.ids_in; a.w_in = f.w_in;
   a.slot_map = f.slot_map;
@@ -1213,18 +1315,7 @@ cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st) {
   a.miss_ids = f.miss_ids; a.n_miss = f.n_miss;
   a.partial = f.partial;
   a.status = f.status; a.sync = f.sync;
-  if (TB == 8) {
-    switch (MT) {
-      case 4: return launch_mt<4, 1>(a, st);
-      case 2: return launch_mt<2, 1>(a, st);
-      default: return launch_mt<1, 1>(a, st);
-    }
-  }
-  switch (MT) {
-    case 4: return launch_mt<4, 2>(a, st);
-    case 2: return launch_mt<2, 2>(a, st);
-    default: return launch_mt<1, 2>(a, st);
-  }
+  return TB == 8 ? launch_nt<1>(a, st) : launch_nt<2>(a, st);
 }
 
 }  // namespace moe

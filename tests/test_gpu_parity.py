@@ -305,22 +305,54 @@ def test_empty_window_is_a_noop():
     assert int(out["n_miss"].item()) == 0
 
 
-def test_deterministic_and_window_composition_invariant():
+@pytest.mark.parametrize("I", [768, 256])
+def test_deterministic_and_window_composition_invariant(I):
     """Same inputs, same bits (run to run); and on the decode path a row's output
-    does not depend on the other rows of its window. (The cut of I into slices
-    follows the window's size class, so the rows compared come from windows of
-    4 or more rows, which are cut alike for this layer.)"""
+    does not depend on the other rows of its window, bit for bit, in windows of
+    1, 2, 4, 8, 12 and 16 rows: alone, a row's groups of I are split into half
+    units, in the 16-row window they are not."""
     cfg = synth.DECODE_WINDOW.with_T(16)
+    if I != cfg.I:
+        cfg = synth.MoeConfig("inv", H=cfg.H, I=I, E=cfg.E, k=cfg.k, T=16, shared_I=I, zipf_s=cfg.zipf_s)
     inp = synth.make_layer(cfg, 11, device=DEV)
     out1, lay = run_layer(inp)
     out2, _ = run_layer(inp, lay=lay)
     assert hashlib.sha256(out1["y"].tobytes()).hexdigest() == hashlib.sha256(out2["y"].tobytes()).hexdigest()
     rng = np.random.default_rng(3)
-    for t, n in ((0, 8), (5, 4), (15, 12)):
+    for t, n in ((0, 8), (5, 4), (15, 12), (3, 1), (9, 1), (7, 2)):
         others = rng.permutation([r for r in range(cfg.T) if r != t])[:n - 1]
         rows = torch.tensor([t, *others.tolist()], dtype=torch.long, device=inp.x.device)
         sub, _ = run_layer(inp, logits=inp.logits[rows], x=inp.x[rows], lay=lay)
-        assert np.array_equal(sub["y"][0], out1["y"][t]), t
+        assert sub["y"][0].tobytes() == out1["y"][t].tobytes(), (t, n)
+
+
+@pytest.mark.parametrize("D", [25, 35])
+def test_split_tail_groups_match_whole_units(D):
+    """A window touching 25 (35) experts has 156 (216) groups of I for 152 SMs:
+    the groups past the first round are split into half units. Its rows are
+    bitwise equal to the same rows computed alone (every group split) and match
+    the oracle."""
+    cfg = synth.DECODE_WINDOW.with_T(8)
+    inp = synth.make_layer(cfg, 21)
+    pool = np.arange(D) * 3
+    stride = (D + cfg.T - 1) // cfg.T
+    ids = np.array([[pool[(stride * t + j) % D] for j in range(cfg.k)] for t in range(cfg.T)], np.int32)
+    assert len(np.unique(ids)) == D
+    rng = np.random.default_rng(5)
+    w = rng.random((cfg.T, cfg.k)).astype(np.float32) + 0.1
+    w = (w / w.sum(1, keepdims=True)).astype(np.float32)
+    dinp = inp.to(DEV)
+    lay = MoeLayer(dinp, T_max=cfg.T)
+    ids_d, w_d = torch.from_numpy(ids).to(DEV), torch.from_numpy(w).to(DEV)
+    y = lay.expert_ffn(dinp.x, ids_d, w_d)["y"].cpu().numpy()
+    torch.cuda.synchronize()
+    code, bits = lay.status()
+    assert code == _lib.MOE_OK, bits
+    for t in range(cfg.T):
+        yt = lay.expert_ffn(dinp.x[t:t + 1], ids_d[t:t + 1], w_d[t:t + 1])["y"].cpu().numpy()
+        assert yt[0].tobytes() == y[t].tobytes(), t
+    L = oracle.Layer(inp)
+    check_y(y, L.rows(ids, w), what="split tail")
 
 
 def test_launch_count_reported():
