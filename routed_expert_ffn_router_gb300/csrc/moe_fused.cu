@@ -463,13 +463,9 @@ struct Producer {
   int ui, pd;      // units taken, units published
   int slot, phase; // ring position of job j (slot = j mod nst, phase = (j / nst) & 1)
 
-  // Publish the units whose partials are all stored (never blocks).
+  // Count the units the consumer warps have published (never blocks).
   __device__ __forceinline__ void poll() {
-    while (pd < ui && mbar_test(pub0 + 8 * (pd % kPubBars), (pd / kPubBars) & 1)) {
-      __threadfence();  // the consumers' partial stores, then the count
-      atomicAdd(a.sync + kSyncUnits, 1);
-      ++pd;
-    }
+    while (pd < ui && mbar_test(pub0 + 8 * (pd % kPubBars), (pd / kPubBars) & 1)) ++pd;
   }
   __device__ __forceinline__ bool timed_out(long long t0) {
     if (cycles_now() - t0 <= kWaitCycles) return false;
@@ -558,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   __shared__ __align__(8) uint64_t s_bar[2 * kMaxNst + kPubBars];  // full, empty, publish
   __shared__ int4 s_hdr[kMaxNst];                           // the job in each stage
   __shared__ uint32_t s_total;
+  __shared__ uint32_t s_wsum[kWarps];  // warp sums of the permutation's prefix sum
   __shared__ int s_abort;
 
   constexpr int MT = kMT, UI = kUI;  // full units; half units have MT = 2
@@ -639,58 +636,67 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   }
   cp_async_wait_all();
   __syncthreads();  // the top-k scratch (stage memory) is released; the slot map is in
-  // ---- permutation: token masks (shared atomics), then one warp builds the
-  // active-expert list (ascending id), the offsets and the miss list
+  // ---- permutation: token masks (shared atomics), then the active-expert
+  // list (ascending id), the offsets and the miss list: one expert per thread,
+  // a prefix sum over the block of (active | misses << 11 | routed rows << 22)
   for (int p = tid; p < T * k; p += kThreads) atomicOr(&s_tokmask[s_ids[p / k][p % k]], 1u << (p / k));
   __syncthreads();
-  if (warp == 1) {
-    const int per = (E + 31) >> 5;
-    const int e0 = lane * per, e1 = min(E, e0 + per);
-    uint32_t pack = 0;  // active count | misses << 11 | routed rows << 22
-    for (int e = e0; e < e1; ++e) {
-      const uint32_t m = s_tokmask[e];
-      if (!m) continue;
-      int slot = s_slot[e];
-      if (slot >= a.S) slot = -1;
-      pack += slot >= 0 ? 1u + ((uint32_t)__popc(m) << 22) : (1u << 11);
-    }
-    uint32_t x = pack;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
-      if (lane >= off) x += y;
-    }
-    const uint32_t tot = __shfl_sync(0xffffffffu, x, 31);
-    const uint32_t ex = x - pack;
-    int ai = ex & 0x7ff, mi = (ex >> 11) & 0x7ff, off = (ex >> 22) & 0x3ff;
-    for (int e = e0; e < e1; ++e) {
-      int16_t dd = -1;
-      const uint32_t m = s_tokmask[e];
-      if (m) {
-        int slot = s_slot[e];
-        if (slot >= a.S) {
-          if (bid == 0) atomicOr(a.status, DEV_BAD_SLOT);
-          slot = -1;
-        }
-        if (slot >= 0) {
-          dd = (int16_t)ai;
-          s_act_e[ai] = (int16_t)e;
-          s_act_slot[ai] = slot;
-          s_act_off[ai] = (int16_t)off;
-          s_act_cnt[ai] = (uint8_t)__popc(m);
-          off += __popc(m);
-          ++ai;
-        } else {
-          if (bid == 0) a.miss_ids[mi] = e;
-          ++mi;
+  {
+    uint32_t base = 0;  // the pack of the experts of earlier rounds
+    for (int r0 = 0; r0 < E; r0 += kThreads) {
+      const int e = r0 + tid;
+      uint32_t m = 0, pack = 0;
+      int slot = -1;
+      if (e < E) {
+        m = s_tokmask[e];
+        if (m) {
+          slot = s_slot[e];
+          if (slot >= a.S) {
+            if (bid == 0) atomicOr(a.status, DEV_BAD_SLOT);
+            slot = -1;
+          }
+          pack = slot >= 0 ? 1u + ((uint32_t)__popc(m) << 22) : (1u << 11);
         }
       }
-      s_d_of_e[e] = dd;
+      uint32_t x = pack;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+      }
+      if (lane == 31) s_wsum[warp] = x;
+      __syncthreads();
+      uint32_t pre = base, rsum = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const uint32_t v = s_wsum[w];
+        pre += w < warp ? v : 0u;
+        rsum += v;
+      }
+      const uint32_t ex = pre + x - pack;
+      if (e < E) {
+        int16_t dd = -1;
+        if (m) {
+          const int ai = ex & 0x7ff, mi = (ex >> 11) & 0x7ff, off = (ex >> 22) & 0x3ff;
+          if (slot >= 0) {
+            dd = (int16_t)ai;
+            s_act_e[ai] = (int16_t)e;
+            s_act_slot[ai] = slot;
+            s_act_off[ai] = (int16_t)off;
+            s_act_cnt[ai] = (uint8_t)__popc(m);
+          } else if (bid == 0) {
+            a.miss_ids[mi] = e;
+          }
+        }
+        s_d_of_e[e] = dd;
+      }
+      base += rsum;
+      __syncthreads();  // s_wsum is read before the next round writes it
     }
-    if (lane == 0) {
-      s_total = tot;
-      const int Dw = tot & 0x7ff, Pw = (tot >> 22) & 0x3ff;
-      if (bid == 0) *a.n_miss = (tot >> 11) & 0x7ff;
+    if (tid == 0) {
+      s_total = base;
+      const int Dw = base & 0x7ff, Pw = (base >> 22) & 0x3ff;
+      if (bid == 0) *a.n_miss = (base >> 11) & 0x7ff;
       if (has_shared) {
         s_act_e[Dw] = -1;
         s_act_slot[Dw] = -1;
@@ -699,7 +705,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
       }
     }
   }
-  __syncthreads();
   __syncthreads();
   const uint32_t tot = s_total;
   Sched sc;
@@ -711,8 +716,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   const int D = sc.D;
   const int nch = H / kKC;        // gate/up jobs (256 columns) per unit
   const int nchd = H / kDnRows;   // down jobs (512 rows) per unit
-  // published units and routing-weight rows the reduction waits for
-  const int target = sc.total + (layer_mode ? T : 0);
+  // the reduction waits for every consumer warp's share of every unit and
+  // for the routing-weight rows
+  const int target = sc.total * kCW + (layer_mode ? T : 0);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -787,6 +793,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     int pub_bar = -1;       // publish barrier of a unit whose partial copies may be in flight
     // A unit is published once its partial copies are complete (checked one
     // job later, when they have long landed): every consumer lane arrives.
+    // Each warp publishes its share with a release add at gpu scope (after
+    // its lanes' copies are complete), and tells the producer's unit ring.
     auto publish = [&]() {
       if (pub_bar < 0) return;
       if (bulk_wr) {
@@ -794,6 +802,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
         fence_proxy_async_global();
         bulk_wr = bulk_rd = false;
       }
+      __syncwarp();
+      if (lane == 0) red_release_gpu_add(a.sync + kSyncUnits, 1);
       mbar_arrive(pub0 + 8 * pub_bar);
       pub_bar = -1;
     };
