@@ -43,6 +43,36 @@ __device__ int block_excl_scan(int v, int* s_warp, int* s_total) {
   return res;
 }
 
+// Stable rank of this thread's pair among the earlier pairs of the 1024-thread
+// block with the same expert e (valid: this thread holds a pair). Warp w
+// counts its pairs per expert with a match (the lowest lane of each expert
+// writes the count into cnt[e][w]); a pair's rank is the sum of its expert's
+// counts in warps before w plus its position among the same-expert lanes of
+// its own warp. cnt: [kMaxE][32] bytes.
+__device__ int block_stable_rank(int e, bool valid, uint8_t (*cnt)[32]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kMaxE * 8; i += blockDim.x) reinterpret_cast<uint32_t*>(cnt)[i] = 0;
+  __syncthreads();
+  const unsigned act = __ballot_sync(0xffffffffu, valid);
+  const unsigned same = __match_any_sync(0xffffffffu, valid ? e : -1) & act;
+  const unsigned lower = same & ((1u << lane) - 1u);
+  if (valid && lower == 0) cnt[e][warp] = (uint8_t)__popc(same);
+  __syncthreads();
+  int r = __popc(lower);
+  if (valid) {
+    const uint4* row = reinterpret_cast<const uint4*>(cnt[e]);
+    const uint4 a = row[0], b = row[1];
+    const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int nb = min(max(warp - 4 * i, 0), 4);  // bytes of this word from warps before ours
+      const uint32_t m = nb == 4 ? 0xffffffffu : ((1u << (8 * nb)) - 1u);
+      r = (int)__dp4a(wd[i] & m, 0x01010101u, (unsigned)r);
+    }
+  }
+  return r;
+}
+
 // Miss list, active-expert records and token-chunk work units, from the
 // per-expert counts and offsets held in shared memory. Thread e handles
 // expert e (blockDim >= E).
@@ -112,18 +142,16 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
                                                              int E, int k,
                                                              const int32_t* __restrict__ slot_map,
                                                              int S, int has_shared, PermuteOut o) {
-  __shared__ int s_ids[kChunk];
   __shared__ int s_cnt[kMaxE];
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_warp[32];
   __shared__ int s_total;
+  __shared__ __align__(16) uint8_t s_rc[kMaxE][32];
   const int tid = threadIdx.x;
   const int P = T * k;
   int e = 0;
-  if (tid < P) {
-    e = load_id(ids, tid, E, o.status);
-    s_ids[tid] = e;
-  }
+  if (tid < P) e = load_id(ids, tid, E, o.status);
+  const int rank = block_stable_rank(e, tid < P, s_rc);
   if (tid < E) s_cnt[tid] = 0;
   __syncthreads();
   if (tid < P) atomicAdd(&s_cnt[e], 1);
@@ -133,8 +161,6 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
   if (tid == 0) s_off[E] = P;
   __syncthreads();
   if (tid < P) {
-    int rank = 0;
-    for (int q = 0; q < tid; ++q) rank += (s_ids[q] == e) ? 1 : 0;
     int pos = s_off[e] + rank;
     o.sorted_pair[pos] = tid;
     o.pair_pos[tid] = pos;
@@ -190,19 +216,14 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int k,
 // Step 3: position = offsets[e] + base of this chunk for e + rank inside the chunk.
 __global__ void __launch_bounds__(1024) permute_scatter_kernel(const int32_t* __restrict__ ids,
                                                                int P, int E, PermuteOut o) {
-  __shared__ int s_ids[kChunk];
+  __shared__ __align__(16) uint8_t s_rc[kMaxE][32];
   const int tid = threadIdx.x;
   const int p0 = blockIdx.x * kChunk;
   const int n = min(kChunk, P - p0);
   int e = 0;
+  if (tid < n) e = load_id(ids, p0 + tid, E, o.status);
+  const int rank = block_stable_rank(e, tid < n, s_rc);
   if (tid < n) {
-    e = load_id(ids, p0 + tid, E, o.status);
-    s_ids[tid] = e;
-  }
-  __syncthreads();
-  if (tid < n) {
-    int rank = 0;
-    for (int q = 0; q < tid; ++q) rank += (s_ids[q] == e) ? 1 : 0;
     int pos = o.offsets[e] + o.hist[(size_t)blockIdx.x * E + e] + rank;
     o.sorted_pair[pos] = p0 + tid;
     o.pair_pos[p0 + tid] = pos;
