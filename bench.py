@@ -235,11 +235,17 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def csrc_hash() -> str:
+# the sources each timed kernel is built from (a change to any of them voids
+# its committed ncu traffic figure)
+KERNEL_SOURCES = {"fused_decode": ("moe_fused.cu", "moe_common.cuh", "moe_internal.h")}
+
+
+def csrc_hash(kernel: str = "fused_decode") -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "routed_expert_ffn_router_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(d, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "moe.h"), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -252,7 +258,7 @@ def ncu_traffic(kernel: str, workload: str):
     try:
         d = json.load(open(p))
         ent = d.get(workload, {}).get(kernel)
-        if ent and ent.get("csrc_sha") == csrc_hash():
+        if ent and ent.get("csrc_sha") == csrc_hash(kernel):
             return ent.get("dram_bytes_per_launch")
     except Exception:
         return None

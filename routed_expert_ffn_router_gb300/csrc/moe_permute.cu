@@ -196,10 +196,16 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int T, int E, int k,
   const int P = T * k;
   int run = 0;
   if (tid < E) {
-    for (int c = 0; c < n_chunks; ++c) {
-      int h = o.hist[(size_t)c * E + tid];
-      o.hist[(size_t)c * E + tid] = run;
-      run += h;
+    // 8 chunks' counts in flight at a time (the loads do not wait for the stores)
+    for (int c0 = 0; c0 < n_chunks; c0 += 8) {
+      int h[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) h[u] = c0 + u < n_chunks ? __ldcg(o.hist + (size_t)(c0 + u) * E + tid) : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + u < n_chunks) o.hist[(size_t)(c0 + u) * E + tid] = run;
+        run += h[u];
+      }
     }
     s_cnt[tid] = run;
   }
