@@ -174,6 +174,210 @@ __device__ __forceinline__ bool mbar_wait_short(uint32_t bar, uint32_t parity, i
   return mbar_wait_sleep(bar, parity, status, 128);
 }
 
+// ---------------------------------------------------------------- top-k
+__device__ __forceinline__ uint32_t order_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u << 1) == 0) u = 0;  // -0 and +0 are equal logits: same key
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+
+// Top-k of one row by one warp. Keys are 64-bit (order_key(logit) << 32 | ~id):
+// unique, and larger means "earlier" (logit descending, ties to the lower id).
+// The k-th largest of the 32 lane maxima bounds the k-th largest key from below
+// (those k maxima are k distinct keys), so only keys at or above it can be
+// selected; they are compacted and ranked by counting. If there are more than
+// kTopkCand candidates (many top keys in few lanes) the warp falls back to k
+// rounds of arg-max. Writes ids[0..k) in order and leaves the ranked keys in
+// scr[kTopkRanked + r]. Returns true if a logit was not finite.
+constexpr int kTopkCand = 256;
+constexpr int kTopkRanked = 32 + kTopkCand;
+constexpr int kTopkScratch = kTopkRanked + 32;  // 64-bit words per warp
+
+template <int NPER>
+__device__ bool topk_row(const float* l, int E, int k, unsigned long long* scr, int* ids) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long key[NPER];
+  unsigned long long mx = 0;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const int e = lane + 32 * i;
+    const float v = e < E ? l[e] : 0.f;
+    if (e < E && !isfinite(v)) bad = true;
+    key[i] = e < E ? (((unsigned long long)order_key(v) << 32) | (uint32_t)(~e)) : 0ull;
+    mx = key[i] > mx ? key[i] : mx;
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  scr[lane] = mx;
+  __syncwarp();
+  int rk = 0;
+#pragma unroll 8
+  for (int i = 0; i < 32; ++i) rk += scr[i] > mx ? 1 : 0;
+  const int kk = k < 32 ? k : 32;
+  const unsigned sel = __ballot_sync(0xffffffffu, rk == kk - 1);
+  const unsigned long long theta = __shfl_sync(0xffffffffu, mx, __ffs(sel) - 1);
+  int c = 0;
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) c += key[i] >= theta ? 1 : 0;
+  int x = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  const int C = __shfl_sync(0xffffffffu, x, 31);
+  unsigned long long* cand = scr + 32;
+  unsigned long long* ranked = scr + kTopkRanked;
+  if (C <= kTopkCand) {
+    int pos = x - c;
+#pragma unroll
+    for (int i = 0; i < NPER; ++i)
+      if (key[i] >= theta) cand[pos++] = key[i];
+    __syncwarp();
+    for (int q = lane; q < C; q += 32) {
+      const unsigned long long me = cand[q];
+      int r = 0;
+      for (int i = 0; i < C; ++i) r += cand[i] > me ? 1 : 0;
+      if (r < k) {
+        ranked[r] = me;
+        ids[r] = (int)(~(uint32_t)me);
+      }
+    }
+  } else {
+    unsigned long long best = 0;
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) best = key[i] > best ? key[i] : best;
+    for (int j = 0; j < k; ++j) {
+      unsigned long long m = best;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, m, off);
+        m = o > m ? o : m;
+      }
+      if (m == best) {
+        best = 0;
+#pragma unroll
+        for (int i = 0; i < NPER; ++i) {
+          if (key[i] == m) key[i] = 0;
+          best = key[i] > best ? key[i] : best;
+        }
+      }
+      if (lane == j) {
+        ranked[j] = m;
+        ids[j] = (int)(~(uint32_t)m);
+      }
+    }
+  }
+  __syncwarp();
+  return bad;
+}
+
+// ---------------------------------------------------------------- routing weights
+// Float-float numbers: an unevaluated sum h + l of two fp32 values (|l| at most
+// half an ulp of h), about 48 significant bits. The error-free sum and product
+// (Knuth's two-sum, Dekker's fast two-sum, the product error from one fused
+// multiply-add) and the composite add and multiply follow the double-double
+// algorithms of Hida, Li and Bailey ("Library for double-double and
+// quad-double arithmetic", 2007), carried over to fp32 pairs.
+struct FF {
+  float h, l;
+};
+__device__ __forceinline__ FF ff_two_sum(float a, float b) {
+  const float s = a + b, bb = s - a;
+  return {s, (a - (s - bb)) + (b - bb)};
+}
+__device__ __forceinline__ FF ff_fast_two_sum(float a, float b) {  // |a| >= |b| (or a = 0)
+  const float s = a + b;
+  return {s, b - (s - a)};
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  FF s = ff_two_sum(a.h, b.h);
+  const FF t = ff_two_sum(a.l, b.l);
+  s.l += t.h;
+  s = ff_fast_two_sum(s.h, s.l);
+  s.l += t.l;
+  return ff_fast_two_sum(s.h, s.l);
+}
+__device__ __forceinline__ FF ff_mul(FF a, FF b) {
+  const float p = a.h * b.h;
+  float e = fmaf(a.h, b.h, -p);
+  e = fmaf(a.h, b.l, e);
+  e = fmaf(a.l, b.h, e);
+  return ff_fast_two_sum(p, e);
+}
+
+// exp(d) = E * 2^n for a float-float d <= 0 with d.h >= -80: n = round(d / ln 2),
+// r = d - n ln 2 with ln 2 = L1 + L2 + L3 (L1 holds 17 significant bits, so n L1
+// is exact; |r| <= ln2 / 2 + tiny), and E = the Taylor series of exp(r) to
+// degree 12 (truncation below 2^-52 for |r| <= 0.35): the terms from r^9 on in
+// fp32, the rest by float-float Horner steps. Coefficients: 1/i! split into
+// two fp32 values.
+__device__ __forceinline__ FF ff_exp_scaled(FF d, int& n_out) {
+  constexpr float kL1 = 0x1.62e4p-1f, kL2 = 0x1.7f7d1cp-20f, kL3 = 0x1.ef357ap-45f;
+  constexpr float kLog2e = 0x1.715476p+0f;
+  const float n = rintf(d.h * kLog2e);
+  const float t = fmaf(-n, kL1, d.h);  // exact: n L1 is exact and close to d.h
+  FF r = ff_two_sum(t, d.l);
+  const float p2 = -n * kL2;
+  r = ff_add(r, FF{p2, fmaf(-n, kL2, -p2)});
+  r = ff_add(r, FF{-n * kL3, 0.f});
+  constexpr float ch[9] = {1.f, 1.f, 0x1p-1f, 0x1.555556p-3f, 0x1.555556p-5f, 0x1.111112p-7f,
+                           0x1.6c16c2p-10f, 0x1.a01a02p-13f, 0x1.a01a02p-16f};
+  constexpr float cl[9] = {0.f, 0.f, 0.f, -0x1.555556p-28f, -0x1.555556p-30f, -0x1.dddddep-32f,
+                           -0x1.27d27ep-35f, -0x1.7f97fap-39f, -0x1.7f97fap-42f};
+  float tail = 0x1.1eed8ep-29f;  // 1/12!
+  tail = fmaf(tail, r.h, 0x1.ae6456p-26f);  // 1/11!
+  tail = fmaf(tail, r.h, 0x1.27e4fcp-22f);  // 1/10!
+  tail = fmaf(tail, r.h, 0x1.71de3ap-19f);  // 1/9!
+  FF acc{tail, 0.f};
+#pragma unroll
+  for (int i = 8; i >= 0; --i) acc = ff_add(ff_mul(acc, r), FF{ch[i], cl[i]});
+  n_out = (int)n;
+  return acc;
+}
+
+// Softmax over the k selected logits of one row, one warp: lane j < k holds
+// logit v_j in rank order (v_0 the largest) and receives
+//   w_j = fp32( exp(v_j - v_0) / sum_{i < k} exp(v_i - v_0) ),  the sum in i order,
+// the reference evaluated in float64. Here in float-float, to about 2^-42
+// relative, so the one rounding to fp32 agrees with float64 except for values
+// within that distance of an fp32 rounding midpoint (float64 itself is slow on
+// this GPU). Rows with a difference below -80 (a weight near fp32 underflow) or
+// a non-finite logit take the float64 evaluation. Call with all 32 lanes.
+__device__ __forceinline__ float topk_softmax_weight_f64(float v, int k) {
+  const int lane = threadIdx.x & 31;
+  const double m0 = (double)__shfl_sync(0xffffffffu, v, 0);
+  const double ej = lane < k ? exp((double)v - m0) : 0.0;
+  double s = 0.0;
+  for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, ej, j);
+  return (float)(ej / s);
+}
+__device__ __forceinline__ float topk_softmax_weight(float v, int k) {
+  const int lane = threadIdx.x & 31;
+  const bool act = lane < k;
+  const float v0 = __shfl_sync(0xffffffffu, v, 0);
+  const FF d = ff_two_sum(v, -v0);  // v - v0, exactly
+  const bool slow = act && !(d.h >= -80.f && d.h <= 0.f && isfinite(d.l));
+  if (__any_sync(0xffffffffu, slow)) return topk_softmax_weight_f64(v, k);
+  int n = 0;
+  FF e{0.f, 0.f};
+  if (act) e = ff_exp_scaled(d, n);
+  const float eh = ldexpf(e.h, n), el = ldexpf(e.l, n);
+  FF s{0.f, 0.f};
+  for (int i = 0; i < k; ++i)
+    s = ff_add(s, FF{__shfl_sync(0xffffffffu, eh, i), __shfl_sync(0xffffffffu, el, i)});
+  // q = e / s: the quotient of the leading parts, corrected by the remainder
+  const float qh = __fdiv_rn(e.h, s.h);
+  const FF p = ff_mul(FF{qh, 0.f}, s);
+  const FF rem = ff_add(e, FF{-p.h, -p.l});
+  const float q = qh + __fdiv_rn(rem.h, s.h);
+  return ldexpf(q, n);  // exact: q 2^n stays a normal fp32 number for n >= -116
+}
+
 // f = (a & b) ^ c
 __device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;

@@ -131,110 +131,10 @@ __host__ __device__ inline size_t smem_bytes(int MT, int NTX, int nst, int stage
 // top-k scratch of every warp), before the first weight copy.
 constexpr int kSlotMapOff = 32768;
 
-__device__ __forceinline__ uint32_t order_key(float v) {
-  uint32_t u = __float_as_uint(v);
-  if ((u << 1) == 0) u = 0;  // -0 and +0 are equal logits: same key
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 // n-th (0-based) set bit of a mask (mask has more than n bits set).
 __device__ __forceinline__ int nth_bit(uint32_t m, int n) {
   for (int i = 0; i < n; ++i) m &= m - 1;
   return __ffs(m) - 1;
-}
-
-// Top-k of one row by one warp. Keys are 64-bit (order_key(logit) << 32 | ~id):
-// unique, and larger means "earlier" (logit descending, ties to the lower id).
-// The k-th largest of the 32 lane maxima bounds the k-th largest key from below
-// (those k maxima are k distinct keys), so only keys at or above it can be
-// selected; they are compacted and ranked by counting. If there are more than
-// kTopkCand candidates (many top keys in few lanes) the warp falls back to k
-// rounds of arg-max. Writes ids[0..k) in order and leaves the ranked keys in
-// scr[kTopkRanked + r]. Returns true if a logit was not finite.
-constexpr int kTopkCand = 256;
-constexpr int kTopkRanked = 32 + kTopkCand;
-constexpr int kTopkScratch = kTopkRanked + 32;  // 64-bit words per warp
-
-template <int NPER>
-__device__ bool topk_row(const float* l, int E, int k, unsigned long long* scr, int* ids) {
-  const int lane = threadIdx.x & 31;
-  unsigned long long key[NPER];
-  unsigned long long mx = 0;
-  bool bad = false;
-#pragma unroll
-  for (int i = 0; i < NPER; ++i) {
-    const int e = lane + 32 * i;
-    const float v = e < E ? l[e] : 0.f;
-    if (e < E && !isfinite(v)) bad = true;
-    key[i] = e < E ? (((unsigned long long)order_key(v) << 32) | (uint32_t)(~e)) : 0ull;
-    mx = key[i] > mx ? key[i] : mx;
-  }
-  bad = __any_sync(0xffffffffu, bad);
-  scr[lane] = mx;
-  __syncwarp();
-  int rk = 0;
-#pragma unroll 8
-  for (int i = 0; i < 32; ++i) rk += scr[i] > mx ? 1 : 0;
-  const int kk = k < 32 ? k : 32;
-  const unsigned sel = __ballot_sync(0xffffffffu, rk == kk - 1);
-  const unsigned long long theta = __shfl_sync(0xffffffffu, mx, __ffs(sel) - 1);
-  int c = 0;
-#pragma unroll
-  for (int i = 0; i < NPER; ++i) c += key[i] >= theta ? 1 : 0;
-  int x = c;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  const int C = __shfl_sync(0xffffffffu, x, 31);
-  unsigned long long* cand = scr + 32;
-  unsigned long long* ranked = scr + kTopkRanked;
-  if (C <= kTopkCand) {
-    int pos = x - c;
-#pragma unroll
-    for (int i = 0; i < NPER; ++i)
-      if (key[i] >= theta) cand[pos++] = key[i];
-    __syncwarp();
-    for (int q = lane; q < C; q += 32) {
-      const unsigned long long me = cand[q];
-      int r = 0;
-      for (int i = 0; i < C; ++i) r += cand[i] > me ? 1 : 0;
-      if (r < k) {
-        ranked[r] = me;
-        ids[r] = (int)(~(uint32_t)me);
-      }
-    }
-  } else {
-    unsigned long long best = 0;
-#pragma unroll
-    for (int i = 0; i < NPER; ++i) best = key[i] > best ? key[i] : best;
-    for (int j = 0; j < k; ++j) {
-      unsigned long long m = best;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, m, off);
-        m = o > m ? o : m;
-      }
-      if (m == best) {
-        best = 0;
-#pragma unroll
-        for (int i = 0; i < NPER; ++i) {
-          if (key[i] == m) key[i] = 0;
-          best = key[i] > best ? key[i] : best;
-        }
-      }
-      if (lane == j) {
-        ranked[j] = m;
-        ids[j] = (int)(~(uint32_t)m);
-      }
-    }
-  }
-  __syncwarp();
-  return bad;
 }
 
 
@@ -763,18 +663,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     __syncwarp();
   } else if (warp == kHelperWarp) {
     // ================= helper: routing weights of row bid =================
-    // float64 softmax over the k selected logits in rank order, one rounding
-    // to fp32; published like a unit (the reduction waits for T of them)
+    // softmax over the k selected logits in rank order, one rounding to fp32;
+    // published like a unit (the reduction waits for T of them)
     if (layer_mode && bid < T) {
       const int t = bid;
       const float v = lane < k ? s_topv[t][lane] : 0.f;
-      const double m0 = (double)__shfl_sync(0xffffffffu, v, 0);
-      const double ej = lane < k ? exp((double)v - m0) : 0.0;
-      double sum = 0.0;
-      for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ej, j);
+      const float wv = topk_softmax_weight(v, k);
       if (lane < k) {
         a.ids_out[(size_t)t * k + lane] = s_ids[t][lane];
-        a.w_out[(size_t)t * k + lane] = (float)(ej / sum);
+        a.w_out[(size_t)t * k + lane] = wv;
       }
       __syncwarp();
       if (lane == 0) {

@@ -4,7 +4,8 @@
 // Routing follows "extended-strata-moe reference", "Routing trace format" (a
 // token's routing is k expert ids plus k fp32 weights) and the top-10-of-512
 // router of the SGLang port post. Order: logit descending, ties to the lower
-// id; weights: softmax over the k selected, float64, one rounding to fp32.
+// id; weights: softmax over the k selected, one rounding to fp32 (float-float
+// arithmetic standing in for float64, see topk_softmax_weight).
 #include "moe_internal.h"
 
 namespace moe {
@@ -28,71 +29,39 @@ __global__ void router_logits_kernel(const void* __restrict__ x, const float* __
   logits[idx] = (float)s;
 }
 
-// One warp per row. Each lane owns experts e = lane + 32*i (i < ceil(E/32));
-// its taken flags live in one register. k rounds of a warp arg-max pick the
-// experts in order; a candidate beats another if its logit is larger, or equal
-// with a lower id. Weights: lane j holds e_j = exp(l_j - l_0) in float64; every
-// lane forms s = e_0 + e_1 + ... in j order through shuffles, then
-// w_j = fp32(e_j / s).
+// One warp per row: topk_row (ids in rank order, ties to the lower id; the
+// threshold of the lane maxima, then ranking by counting), then
+// topk_softmax_weight with lane j holding the j-th pick's logit.
+template <int NPER>
+__device__ __forceinline__ void route_row(const float* l, int E, int k, unsigned long long* scr, int* sid,
+                                          int32_t* ids, float* w, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const bool bad = topk_row<NPER>(l, E, k, scr, sid);
+  if (bad && lane == 0 && status) atomicOr(status, DEV_NONFINITE_LOGIT);
+  const float v = lane < k ? key_value((uint32_t)(scr[kTopkRanked + lane] >> 32)) : 0.f;
+  const float wv = topk_softmax_weight(v, k);
+  if (lane < k) {
+    ids[lane] = sid[lane];
+    w[lane] = wv;
+  }
+}
+
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T, int E,
                                                     int k, int32_t* __restrict__ ids,
                                                     float* __restrict__ w,
                                                     int32_t* __restrict__ status) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  __shared__ unsigned long long s_scr[8][kTopkScratch];
+  __shared__ int s_id[8][kMaxK];
+  const int wp = threadIdx.x >> 5;
+  const int t = blockIdx.x * 8 + wp;
   if (t >= T) return;
   const float* l = logits + (size_t)t * E;
-  const int nper = (E + 31) >> 5;  // <= 32
-  float v[32];
-  bool bad = false;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    int e = lane + 32 * i;
-    v[i] = (i < nper && e < E) ? l[e] : 0.f;
-    if (i < nper && e < E && !isfinite(v[i])) bad = true;
-  }
-  if (__any_sync(0xffffffffu, bad) && lane == 0 && status) atomicOr(status, DEV_NONFINITE_LOGIT);
-  uint32_t taken = 0;
-  float my_v = 0.f;
-  int my_e = 0;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      int e = lane + 32 * i;
-      if (i < nper && e < E && !((taken >> i) & 1u)) {
-        if (be == 0x7fffffff || v[i] > bv) {  // ascending e: strict '>' keeps the lower id
-          bv = v[i];
-          be = e;
-        }
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      bool take = (be == 0x7fffffff) || (oe != 0x7fffffff && (ov > bv || (ov == bv && oe < be)));
-      if (take) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if (be == 0x7fffffff) be = 0;  // only with non-finite input (already flagged)
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == j) {
-      my_v = bv;
-      my_e = be;
-    }
-  }
-  const double m = (double)__shfl_sync(0xffffffffu, my_v, 0);
-  double ej = (lane < k) ? exp((double)my_v - m) : 0.0;
-  double s = 0.0;
-  for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, ej, j);
-  if (lane < k) {
-    ids[(size_t)t * k + lane] = my_e;
-    w[(size_t)t * k + lane] = (float)(ej / s);
-  }
+  int32_t* ir = ids + (size_t)t * k;
+  float* wr = w + (size_t)t * k;
+  if (E <= 128) route_row<4>(l, E, k, s_scr[wp], s_id[wp], ir, wr, status);
+  else if (E <= 256) route_row<8>(l, E, k, s_scr[wp], s_id[wp], ir, wr, status);
+  else if (E <= 512) route_row<16>(l, E, k, s_scr[wp], s_id[wp], ir, wr, status);
+  else route_row<32>(l, E, k, s_scr[wp], s_id[wp], ir, wr, status);
 }
 
 cudaError_t launch_router_logits(const void* x, bool x_bf16, const float* wg, int T, int H, int E,

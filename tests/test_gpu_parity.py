@@ -91,6 +91,19 @@ def test_route_bit_exact(name, T, E, k, s):
     assert_weights_match(w, w_o, we)
 
 
+@pytest.mark.parametrize("sigma", [0.01, 1.0, 12.0, 40.0])
+def test_route_weights_many_rows(sigma):
+    """Weights of 40,000 rows against the float64 oracle, logits spread from
+    nearly equal to differences past 80 (the float64 fallback)."""
+    rng = np.random.default_rng(int(sigma * 100) + 1)
+    lg = (rng.normal(size=(40000, 64)) * sigma).astype(np.float32)
+    ids_o, w_o, we = oracle.route(lg, 8)
+    ids, w, st = gpu_route(lg, 8)
+    assert st == 0
+    assert np.array_equal(ids, ids_o)
+    assert_weights_match(w, w_o, we)
+
+
 def test_route_ties_go_to_lower_id():
     rng = np.random.default_rng(3)
     lg = (np.round(rng.normal(size=(300, 64)) * 2) / 2).astype(np.float32)  # many exact ties
