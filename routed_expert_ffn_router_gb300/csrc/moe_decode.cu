@@ -376,20 +376,39 @@ __global__ void __launch_bounds__(256) down_kernel(FfnArgs a) {
 }
 
 // y[t] = sum_{j<k, resident} partial[pair_pos[t*k+j]] (j order) + partial[P+t].
+// The routing entries and partial rows of 8 picks are loaded before any is
+// summed, so a thread has 8 partial loads in flight instead of one.
 __global__ void __launch_bounds__(256) combine_kernel(FfnArgs a, int has_shared) {
   const int t = blockIdx.y;
   const int c4 = blockIdx.x * 256 + threadIdx.x;
   if (c4 * 4 >= a.H) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < a.k; ++j) {
-    const int p = t * a.k + j;
-    const int e = a.ids[p];
-    if (e < 0 || e >= a.E) continue;
-    const int slot = a.slot_map ? a.slot_map[e] : e;
-    if (slot < 0 || slot >= a.S) continue;
-    const float4 v =
-        *reinterpret_cast<const float4*>(a.partial + (size_t)a.pair_pos[p] * a.H + (size_t)c4 * 4);
-    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = 0; j0 < a.k; j0 += 8) {
+    int pos[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      pos[u] = -1;
+      const int j = j0 + u;
+      if (j < a.k) {
+        const int p = t * a.k + j;
+        const int e = a.ids[p];
+        if (e >= 0 && e < a.E) {
+          const int slot = a.slot_map ? a.slot_map[e] : e;
+          if (slot >= 0 && slot < a.S) pos[u] = a.pair_pos[p];
+        }
+      }
+    }
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v[u] = pos[u] >= 0 ? *reinterpret_cast<const float4*>(a.partial + (size_t)pos[u] * a.H + (size_t)c4 * 4)
+                         : zero;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (pos[u] >= 0) {
+        acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
+      }
   }
   if (has_shared) {
     const float4 v =

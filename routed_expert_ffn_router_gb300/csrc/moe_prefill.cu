@@ -324,18 +324,25 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
         const int spb = 8 >> jb.bsel;
         const uint32_t bbytes = (16u << jb.bsel) * 128;
         bool ok = true;
+        // descriptors of the first A and B tiles; the others differ by their
+        // address / 16 in the low field (no carry: shared addresses < 256 KB)
+        const uint64_t ad0 = sdesc_sw128(sA), bd0 = sdesc_sw128(sB);
         for (int kb = 0; kb < nkb; ++kb) {
           const int as = acnt % kASt, bs = bcnt % kBSt, u = kb % spb;
-          ok = mbar_wait_short(a_full + 8 * as, (acnt / kASt) & 1, a.status) &&
-               (u != 0 || mbar_wait_short(b_full + 8 * bs, (bcnt / kBSt) & 1, a.status));
+          // a ready stage is the common case: test once before the sleeping wait
+          ok = (mbar_test(a_full + 8 * as, (acnt / kASt) & 1) ||
+                mbar_wait_short(a_full + 8 * as, (acnt / kASt) & 1, a.status)) &&
+               (u != 0 || mbar_test(b_full + 8 * bs, (bcnt / kBSt) & 1) ||
+                mbar_wait_short(b_full + 8 * bs, (bcnt / kBSt) & 1, a.status));
           if (!ok) break;
           tc_fence_after();
+          const uint64_t bdk = bd0 + ((uint32_t)(bs * kBTile + u * bbytes) >> 4);
+          const uint64_t adk = ad0 + ((uint32_t)(as * NM * kATile) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sdesc_sw128(sB + bs * kBTile + u * bbytes + kk * 32);
 #pragma unroll
             for (int m = 0; m < NM; ++m)
-              tc_mma(tmem + ab * 256 + m * 128, sdesc_sw128(sA + (as * NM + m) * kATile + kk * 32), bd, idesc,
+              tc_mma(tmem + ab * 256 + m * 128, adk + ((m * kATile + kk * 32) >> 4), bdk + ((kk * 32) >> 4), idesc,
                      (kb > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(a_empty + 8 * as);  // the tiles are free once these MMAs are done
