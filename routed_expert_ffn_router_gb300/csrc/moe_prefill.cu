@@ -327,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
         // descriptors of the first A and B tiles; the others differ by their
         // address / 16 in the low field (no carry: shared addresses < 256 KB)
         const uint64_t ad0 = sdesc_sw128(sA), bd0 = sdesc_sw128(sB);
-        for (int kb = 0; kb < nkb; ++kb) {
-          const int as = acnt % kASt, bs = bcnt % kBSt, u = kb % spb;
+        for (int kb = 0, u = 0; kb < nkb; ++kb) {  // u = kb mod spb (a power of two)
+          const int as = acnt % kASt, bs = bcnt % kBSt;
           // a ready stage is the common case: test once before the sleeping wait
           ok = (mbar_test(a_full + 8 * as, (acnt / kASt) & 1) ||
                 mbar_wait_short(a_full + 8 * as, (acnt / kASt) & 1, a.status)) &&
@@ -347,9 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
           }
           tc_commit(a_empty + 8 * as);  // the tiles are free once these MMAs are done
           ++acnt;
-          if (u == spb - 1) {
+          if (++u == spb) {
             tc_commit(b_empty + 8 * bs);
             ++bcnt;
+            u = 0;
           }
         }
         if (!ok) {
