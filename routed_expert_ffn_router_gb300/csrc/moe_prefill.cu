@@ -17,9 +17,13 @@
 //   warps 4-11 dequantise a raw stage into fp16 A tiles (128 rows x 64, K-major,
 //   128-byte swizzle): q = (1024 + (q ^ 8)) - 1032 exactly, then q * s with the
 //   fp16 scale, rounded once (2^-12);
-//   warp 14 (one thread) issues tcgen05.mma (M = 128, N = the job's tokens
-//   rounded up to 16, K = 16 per instruction) into one of two TMEM buffers and
-//   commits each stage back to its producers;
+//   warps 14 and 15 (one thread each) issue tcgen05.mma (M = 128, N = the job's
+//   tokens rounded up to 16, K = 16 per instruction), each for one of the two
+//   A tiles of a stage, into one of two TMEM buffers, and commit each stage
+//   back to its producers. A tcgen05.mma holds its issuing thread for about
+//   200 cycles whatever its N (measured on GB300), so one thread cannot keep
+//   the tensor pipe busy at the few-token N of most experts: two issuers halve
+//   the issue time of a step;
 //   warps 0-3 (one TMEM lane quarter each) drain the accumulators: h =
 //   silu(g) u in fp16 (gate/up), or w * (W_d h) as fp32 partials (down).
 // Both operands are fp16: the tensor cores take one type for A and B, and fp16
@@ -48,7 +52,8 @@ namespace pf {
 constexpr int kBM = 128;              // weight rows per job (M of the MMA)
 constexpr int kNT = 128;              // tokens per job at most (N of the MMA)
 constexpr int kRawSt = 2, kASt = 2, kBSt = 4;
-constexpr int kThreads = 480;         // warps 0-3 epilogue, 4-11 dequant, 12-13 producers, 14 MMA
+constexpr int kThreads = 512;         // warps 0-3 epilogue, 4-11 dequant, 12-13 producers, 14-15 MMA
+constexpr int kMmaWarps = 2;          // MMA issuers: one per A tile of a stage
 constexpr int kDq = 256;              // dequantising threads
 constexpr int kMaxAct = kMaxE + 1;
 constexpr int kCodeBox = 128 * 128;   // one raw code box: 128 rows x 128 bytes (256 columns)
@@ -97,13 +102,27 @@ __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
 }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
-      "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
+// The issue forms used by the MMA warps: the whole warp runs the issue loop
+// (its operands stay warp-uniform) and the elected lane issues (lead != 0).
+// Measured on GB300: a converged warp with an elected issuer takes about two
+// thirds of the issue time of a lone lane in a divergent branch.
+__device__ __forceinline__ uint32_t elect_lane() {
+  uint32_t r;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}" : "=r"(r));
+  return r;
 }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+__device__ __forceinline__ void tc_mma_el(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc,
+                                          uint32_t lead) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(acc), "r"(lead));
+}
+__device__ __forceinline__ void tc_commit_el(uint32_t bar, uint32_t lead) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %1, 0;\n"
+      " @q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar), "r"(lead)
+      : "memory");
 }
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
@@ -173,14 +192,14 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     }
     for (int i = 0; i < kASt; ++i) {
       mbar_init(a_full + 8 * i, kDq / 32);
-      mbar_init(a_empty + 8 * i, 1);
+      mbar_init(a_empty + 8 * i, kMmaWarps);
     }
     for (int i = 0; i < kBSt; ++i) {
       mbar_init(b_full + 8 * i, 1);
-      mbar_init(b_empty + 8 * i, 1);
+      mbar_init(b_empty + 8 * i, kMmaWarps);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(acc_full + 8 * i, 1);
+      mbar_init(acc_full + 8 * i, kMmaWarps);
       mbar_init(acc_empty + 8 * i, 4);
     }
     fence_barrier_init();
@@ -307,14 +326,16 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       }
     }
     __syncwarp();
-  } else if (warp == 14) {
-    // ================= MMA issuer =================
-    if (lane == 0) {
+  } else if (warp >= 14) {
+    // ================= MMA issuers: warp 14 + m issues the MMAs of A tile m =================
+    const int m = warp - 14;
+    {
+      const uint32_t lead = elect_lane();
       int acnt = 0, bcnt = 0, jcnt = 0;
       for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
         const Job jb = job_of(j);
         const int ab = jcnt & 1;
-        if (!mbar_wait_short(acc_empty + 8 * ab, ((jcnt >> 1) & 1) ^ 1, a.status)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_short(acc_empty + 8 * ab, ((jcnt >> 1) & 1) ^ 1, a.status))) {
           *abort_flag = 1;
           break;
         }
@@ -334,21 +355,18 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
                 mbar_wait_short(a_full + 8 * as, (acnt / kASt) & 1, a.status)) &&
                (u != 0 || mbar_test(b_full + 8 * bs, (bcnt / kBSt) & 1) ||
                 mbar_wait_short(b_full + 8 * bs, (bcnt / kBSt) & 1, a.status));
-          if (!ok) break;
+          if (!(ok = __all_sync(0xffffffffu, ok))) break;
           tc_fence_after();
           const uint64_t bdk = bd0 + ((uint32_t)(bs * kBTile + u * bbytes) >> 4);
           const uint64_t adk = ad0 + ((uint32_t)(as * NM * kATile) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-            for (int m = 0; m < NM; ++m)
-              tc_mma(tmem + ab * 256 + m * 128, adk + ((m * kATile + kk * 32) >> 4), bdk + ((kk * 32) >> 4), idesc,
-                     (kb > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(a_empty + 8 * as);  // the tiles are free once these MMAs are done
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_el(tmem + ab * 256 + m * 128, adk + ((m * kATile + kk * 32) >> 4), bdk + ((kk * 32) >> 4), idesc,
+                      (kb > 0 || kk > 0) ? 1u : 0u, lead);
+          tc_commit_el(a_empty + 8 * as, lead);  // the tiles are free once these MMAs are done
           ++acnt;
           if (++u == spb) {
-            tc_commit(b_empty + 8 * bs);
+            tc_commit_el(b_empty + 8 * bs, lead);
             ++bcnt;
             u = 0;
           }
@@ -357,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
           *abort_flag = 1;
           break;
         }
-        tc_commit(acc_full + 8 * ab);  // the job's accumulators are complete
+        tc_commit_el(acc_full + 8 * ab, lead);  // the job's accumulators are complete
       }
     }
     __syncwarp();
