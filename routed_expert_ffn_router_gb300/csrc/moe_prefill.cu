@@ -10,22 +10,25 @@
 //
 // Two persistent kernels, one per GEMM, each a warp-specialised pipeline:
 //   warp 12 (one thread) streams a job's int4 codes and fp16 scales (TMA tensor
-//   copies, 256 columns of K per raw stage), warp 13 (one thread) its B
-//   operand (TMA boxes of its rows of the expert-sorted x or h, 64 columns of
-//   K each; a 16 KB B slot holds 1, 2, 4 or 8 of them for 128, 64, 32 or 16
-//   rows, so that jobs with few tokens keep more of K in flight);
-//   warps 4-11 dequantise a raw stage into fp16 A tiles (128 rows x 64, K-major,
-//   128-byte swizzle): q = (1024 + (q ^ 8)) - 1032 exactly, then q * s with the
-//   fp16 scale, rounded once (2^-12);
-//   warps 14 and 15 (one thread each) issue tcgen05.mma (M = 128, N = the job's
-//   tokens rounded up to 16, K = 16 per instruction), each for one of the two
-//   A tiles of a stage, into one of two TMEM buffers, and commit each stage
-//   back to its producers. A tcgen05.mma holds its issuing thread for about
-//   200 cycles whatever its N (measured on GB300), so one thread cannot keep
-//   the tensor pipe busy at the few-token N of most experts: two issuers halve
-//   the issue time of a step;
-//   warps 0-3 (one TMEM lane quarter each) drain the accumulators: h =
-//   silu(g) u in fp16 (gate/up), or w * (W_d h) as fp32 partials (down).
+//   copies, 256 columns of K per raw stage);
+//   warps 4-11 dequantise a raw stage into the job's fp16 weight tile (256
+//   rows x 64 columns of K per step, K-major, 128-byte swizzle): q = (1024 +
+//   (q ^ 8)) - 1032 exactly, then q * s with the fp16 scale, rounded once
+//   (2^-12);
+//   warp 13 (one thread) streams the job's token rows of the expert-sorted x
+//   or h into a 128-row tile per step (a TMA box of 16, 32, 64 or 128 rows by
+//   the job's token count; the stale rows below it only reach accumulator
+//   lanes that are never read);
+//   warp 14 (the whole warp, its elected lane issuing) runs tcgen05.mma with
+//   the token tile as A (M = 128) and the weight tile as B (N = 256), K = 16,
+//   into one of two TMEM accumulators, and commits each stage back to its
+//   producers. Measured on GB300, a tcgen05.mma costs about 200 cycles of the
+//   tensor pipe in a stream with commits, whatever its N: the cost of these
+//   GEMMs is their number of MMAs, so each MMA takes the largest operand shape
+//   (tokens as M, 256 weight rows as N), half as many as with the weights as M;
+//   warps 0-3 (TMEM lanes = tokens) drain the accumulators: each thread holds
+//   one token's 256 weight rows and writes h = silu(g) u in fp16 (gate/up) or
+//   w * (W_d h) as fp32 partials (down) as contiguous rows.
 // Both operands are fp16: the tensor cores take one type for A and B, and fp16
 // keeps q * s and h to 2^-12 where bf16 would round to 2^-9. x enters as
 // x / 2^e_t in fp16, written once per routed pair in the expert-sorted row
@@ -52,14 +55,15 @@ namespace pf {
 constexpr int kBM = 128;              // weight rows per job (M of the MMA)
 constexpr int kNT = 128;              // tokens per job at most (N of the MMA)
 constexpr int kRawSt = 2, kASt = 2, kBSt = 4;
-constexpr int kThreads = 512;         // warps 0-3 epilogue, 4-11 dequant, 12-13 producers, 14-15 MMA
-constexpr int kMmaWarps = 2;          // MMA issuers: one per A tile of a stage
-constexpr int kDq = 256;              // dequantising threads
+// warps 0-3 and 15-18 epilogue, 4-11 and 19-26 dequant, 12-13 producers, 14 MMA
+constexpr int kThreads = 864;
+constexpr int kDqWarps = 16;          // 8 per weight tile: one 16-row band each
+constexpr int kEpiWarps = 8;          // two per TMEM lane quarter, each for half of the weight rows
 constexpr int kMaxAct = kMaxE + 1;
 constexpr int kCodeBox = 128 * 128;   // one raw code box: 128 rows x 128 bytes (256 columns)
 constexpr int kScaleBox = 128 * 16;   // one raw scale box: 128 rows x 8 fp16
-constexpr int kATile = 128 * 128;     // one fp16 A tile: 128 rows x 64 columns
-constexpr int kBTile = kNT * 128;     // one fp16 B tile: up to 128 rows x 64 columns
+constexpr int kATile = 128 * 128;     // one fp16 weight tile: 128 rows x 64 columns (two per step)
+constexpr int kBTile = kNT * 128;     // one fp16 token tile: 128 rows x 64 columns
 
 struct Args {
   CUtensorMap tm_c[2], tm_s[2];       // routed codes / scales (gate, up; or down)
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
   __shared__ __align__(8) uint64_t s_bar[2 * kRawSt + 2 * kASt + 2 * kBSt + 4];
   __shared__ int s_js[kMaxAct + 1];      // first job of each active entry
   __shared__ int s_off[kMaxAct], s_cnt[kMaxAct], s_slot[kMaxAct];
-  __shared__ float s_colf[2][kNT];       // per token column: x prescale (gate/up) or routing weight (down)
+  __shared__ float s_colf[2][kNT];       // down: the routing weight of each token column of a job
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -174,9 +178,11 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
   const int G = gridDim.x, bid = blockIdx.x;
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
-  const uint32_t sraw = smem_u32(smem);
+  // token ring first: a step's 128-row tile may start inside the last slot and
+  // read past the ring's end, into the raw ring (those rows are never used)
+  const uint32_t sB = smem_u32(smem);
+  const uint32_t sraw = sB + kBSt * kBTile;
   const uint32_t sA = sraw + kRawSt * raw_bytes<GU>();
-  const uint32_t sB = sA + kASt * NM * kATile;
   const uint32_t bar0 = smem_u32(&s_bar[0]);
   const uint32_t raw_full = bar0, raw_empty = raw_full + 8 * kRawSt;
   const uint32_t a_full = raw_empty + 8 * kRawSt, a_empty = a_full + 8 * kASt;
@@ -188,19 +194,19 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     s_abort = 0;
     for (int i = 0; i < kRawSt; ++i) {
       mbar_init(raw_full + 8 * i, 1);
-      mbar_init(raw_empty + 8 * i, kDq / 32);  // one arrival per dequantising warp
+      mbar_init(raw_empty + 8 * i, kDqWarps);  // one arrival per dequantising warp
     }
     for (int i = 0; i < kASt; ++i) {
-      mbar_init(a_full + 8 * i, kDq / 32);
-      mbar_init(a_empty + 8 * i, kMmaWarps);
+      mbar_init(a_full + 8 * i, kDqWarps);
+      mbar_init(a_empty + 8 * i, 1);
     }
     for (int i = 0; i < kBSt; ++i) {
       mbar_init(b_full + 8 * i, 1);
-      mbar_init(b_empty + 8 * i, kMmaWarps);
+      mbar_init(b_empty + 8 * i, 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(acc_full + 8 * i, kMmaWarps);
-      mbar_init(acc_empty + 8 * i, 4);
+      mbar_init(acc_full + 8 * i, 1);
+      mbar_init(acc_empty + 8 * i, kEpiWarps);
     }
     fence_barrier_init();
   }
@@ -300,7 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     }
     __syncwarp();
   } else if (warp == 13) {
-    // ================= B producer: expert-sorted rows of x or h =================
+    // ================= token producer: the job's rows of x or h =================
+    // a 16 KB slot holds the boxes of 8 >> bsel consecutive steps (16 << bsel
+    // rows each); the 128-row tile of a step starts at its box, and the rows
+    // after the box (later steps' boxes, stale data) only reach accumulator
+    // lanes that are never read
     if (lane == 0) {
       int bcnt = 0;
       for (int j = bid; j < njobs && !*abort_flag; j += G) {
@@ -312,8 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
           const int bs = bcnt % kBSt;
           if (!(ok = mbar_wait_short(b_empty + 8 * bs, ((bcnt / kBSt) & 1) ^ 1, a.status))) break;
           const uint32_t dst = sB + bs * kBTile, bb = b_full + 8 * bs;
-          // rows past the expert's (other experts' rows, or zeros past the end)
-          // only feed columns that are never stored
           mbar_expect_tx(bb, bbytes * spb);
           for (int u = 0; u < spb; ++u)
             tma_load_2d(dst + u * bbytes, &a.tm_b[jb.bsel], (kb + u) * 64, jb.off + jb.n0, bb);
@@ -326,63 +334,76 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       }
     }
     __syncwarp();
-  } else if (warp >= 14) {
-    // ================= MMA issuers: warp 14 + m issues the MMAs of A tile m =================
-    const int m = warp - 14;
-    {
-      const uint32_t lead = elect_lane();
-      int acnt = 0, bcnt = 0, jcnt = 0;
-      for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
-        const Job jb = job_of(j);
-        const int ab = jcnt & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait_short(acc_empty + 8 * ab, ((jcnt >> 1) & 1) ^ 1, a.status))) {
-          *abort_flag = 1;
-          break;
-        }
+  } else if (warp == 14) {
+    // ================= MMA issuer (whole warp, elected lane issues) =================
+    // D[token][weight row] += X(128 x 16) . W(256 x 16)^T: four MMAs per step
+    const uint32_t lead = elect_lane();
+    // descriptors of the first tiles; the others differ by their address / 16
+    // in the low field (no carry: shared addresses < 256 KB)
+    const uint64_t xd0 = sdesc_sw128(sB), wd0 = sdesc_sw128(sA);
+    int acnt = 0, bcnt = 0, jcnt = 0;
+    for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
+      const Job jb = job_of(j);
+      const int ab = jcnt & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_short(acc_empty + 8 * ab, ((jcnt >> 1) & 1) ^ 1, a.status))) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int nkb = k_of(jb) / 64;
+      const int spb = 8 >> jb.bsel;
+      const uint32_t bbytes = (16u << jb.bsel) * 128;
+      // gate/up: tokens as A (M = 128), the 256 weight rows as B (N = 256);
+      // down: each 128-row weight tile as A, the job's tokens as B (N = np)
+      const uint32_t idesc = GU ? idesc_f16(kNT, 2 * kBM) : idesc_f16(kBM, jb.np);
+      bool ok = true;
+      for (int kb = 0, u = 0; kb < nkb; ++kb) {  // u = kb mod spb (a power of two)
+        const int as = acnt % kASt, bs = bcnt % kBSt;
+        // a ready stage is the common case: test once before the sleeping wait
+        ok = (mbar_test(a_full + 8 * as, (acnt / kASt) & 1) ||
+              mbar_wait_short(a_full + 8 * as, (acnt / kASt) & 1, a.status)) &&
+             (u != 0 || mbar_test(b_full + 8 * bs, (bcnt / kBSt) & 1) ||
+              mbar_wait_short(b_full + 8 * bs, (bcnt / kBSt) & 1, a.status));
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
         tc_fence_after();
-        const uint32_t idesc = idesc_f16(kBM, jb.np);
-        const int nkb = k_of(jb) / 64;
-        const int spb = 8 >> jb.bsel;
-        const uint32_t bbytes = (16u << jb.bsel) * 128;
-        bool ok = true;
-        // descriptors of the first A and B tiles; the others differ by their
-        // address / 16 in the low field (no carry: shared addresses < 256 KB)
-        const uint64_t ad0 = sdesc_sw128(sA), bd0 = sdesc_sw128(sB);
-        for (int kb = 0, u = 0; kb < nkb; ++kb) {  // u = kb mod spb (a power of two)
-          const int as = acnt % kASt, bs = bcnt % kBSt;
-          // a ready stage is the common case: test once before the sleeping wait
-          ok = (mbar_test(a_full + 8 * as, (acnt / kASt) & 1) ||
-                mbar_wait_short(a_full + 8 * as, (acnt / kASt) & 1, a.status)) &&
-               (u != 0 || mbar_test(b_full + 8 * bs, (bcnt / kBSt) & 1) ||
-                mbar_wait_short(b_full + 8 * bs, (bcnt / kBSt) & 1, a.status));
-          if (!(ok = __all_sync(0xffffffffu, ok))) break;
-          tc_fence_after();
-          const uint64_t bdk = bd0 + ((uint32_t)(bs * kBTile + u * bbytes) >> 4);
-          const uint64_t adk = ad0 + ((uint32_t)(as * NM * kATile) >> 4);
+        const uint64_t xdk = xd0 + ((uint32_t)(bs * kBTile + u * bbytes) >> 4);
+        const uint64_t wdk = wd0 + ((uint32_t)(as * NM * kATile) >> 4);
+        if constexpr (GU) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_el(tmem + ab * 256 + m * 128, adk + ((m * kATile + kk * 32) >> 4), bdk + ((kk * 32) >> 4), idesc,
+            tc_mma_el(tmem + ab * 256, xdk + ((kk * 32) >> 4), wdk + ((kk * 32) >> 4), idesc,
                       (kb > 0 || kk > 0) ? 1u : 0u, lead);
-          tc_commit_el(a_empty + 8 * as, lead);  // the tiles are free once these MMAs are done
-          ++acnt;
-          if (++u == spb) {
-            tc_commit_el(b_empty + 8 * bs, lead);
-            ++bcnt;
-            u = 0;
-          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int m = 0; m < NM; ++m)
+              tc_mma_el(tmem + ab * 256 + m * 128, wdk + ((m * kATile + kk * 32) >> 4), xdk + ((kk * 32) >> 4),
+                        idesc, (kb > 0 || kk > 0) ? 1u : 0u, lead);
         }
-        if (!ok) {
-          *abort_flag = 1;
-          break;
+        tc_commit_el(a_empty + 8 * as, lead);  // the tiles are free once these MMAs are done
+        ++acnt;
+        if (++u == spb) {
+          tc_commit_el(b_empty + 8 * bs, lead);
+          ++bcnt;
+          u = 0;
         }
-        tc_commit_el(acc_full + 8 * ab, lead);  // the job's accumulators are complete
       }
+      if (!ok) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_commit_el(acc_full + 8 * ab, lead);  // the job's accumulators are complete
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // ================= dequantisation (warps 4-11: matrix or row tile m = wd / 4) =================
-    const int wd = warp - 4, m = wd >> 2;
-    const int h = lane & 1;
+  } else if ((warp >= 4 && warp <= 11) || warp >= 19) {
+    // ================= dequantisation (16 warps: tile m = wd / 8, rows 16 (wd mod 8) ..) =================
+    // Thread: row r, 32-column block h of each 64-column step. The 8 lanes of a
+    // quarter-warp read 8 consecutive rows of one block: 8 different 16-byte
+    // chunks of the swizzled raw rows, no bank conflict.
+    const int wd = warp <= 11 ? warp - 4 : warp - 11, m = wd >> 3;
+    const int h = lane >> 4;
+    const int r = (wd & 7) * 16 + (lane & 15);
     int rcnt = 0, acnt = 0;
     for (int j = bid; j < njobs && !*abort_flag; j += G) {
       const Job jb = job_of(j);
@@ -396,9 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
           const int as = acnt % kASt;
           if (!(ok = mbar_wait_short(a_empty + 8 * as, ((acnt / kASt) & 1) ^ 1, a.status))) break;
           const int c = 2 * s4 + h;  // 32-column block of the raw stage
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-              const int r = q * 64 + (wd & 3) * 16 + (lane >> 1);
+          {
               const uint4 cw = ld_s128(st + m * kCodeBox + r * 128 + ((c ^ (r & 7)) << 4));
               const uint32_t sh = ld_s32(st + NM * kCodeBox + m * kScaleBox + r * 16 + (c & ~1) * 2);
               const uint32_t s1 = (c & 1) ? (sh >> 16) : (sh & 0xFFFFu);
@@ -426,56 +445,96 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       if (!ok) *abort_flag = 1;
     }
   } else {
-    // ================= epilogue (warps 0-3: TMEM lanes 32w..32w+31) =================
-    const int row = warp * 32 + lane;
+    // ================= epilogue (warps 0-3 and 15-18) =================
+    // A warp reaches the TMEM lane quarter warp mod 4; the two warps of a
+    // quarter split the accumulator's columns (gate/up) or its two weight row
+    // tiles (down).
+    const int qw = warp & 3, half = warp >= 15 ? 1 : 0;
     int jcnt = 0;
+    if constexpr (GU) {
+    // Gate/up: thread = one token of the job (TMEM lane); its accumulator row
+    // holds the 128 gate rows at columns 0-127 and the same up rows at 128-255,
+    // and h goes out as a contiguous fp16 row segment.
+    const int t = qw * 32 + lane;
     for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
       const Job jb = job_of(j);
       const int ab = jcnt & 1;
-      // per-column data, fetched while the job's MMAs run: the x prescale of the
-      // column's token (gate/up) or the routing weight of its pair (down)
-      float* colf = s_colf[ab];
-      if (row < jb.nn) {
-        const int s = jb.off + jb.n0 + row;
-        if (GU) colf[row] = jb.sh ? __ldg(a.xscale + (s - P)) : __ldg(a.xscale + a.sorted_pair[s] / a.k);
-        else colf[row] = jb.sh ? 1.0f : __ldg(a.w + a.sorted_pair[s]);
-      }
-      named_bar_sync(1, 128);
-      if (!mbar_wait_short(acc_full + 8 * ab, (jcnt >> 1) & 1, a.status)) {
+      const bool valid = t < jb.nn;
+      const size_t s = (size_t)jb.off + jb.n0 + (valid ? t : 0);  // the token's expert-sorted row
+      // the token's x prescale, fetched while the job's MMAs run
+      const float cf = !valid ? 0.f : jb.sh ? __ldg(a.xscale + (s - P)) : __ldg(a.xscale + a.sorted_pair[s] / a.k);
+      if (!__all_sync(0xffffffffu, mbar_wait_short(acc_full + 8 * ab, (jcnt >> 1) & 1, a.status))) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + ab * 256;
-      bool range_ok = true;
-      for (int c0 = 0; c0 < jb.np; c0 += 16) {
-        uint32_t g[16], u[16];  // gate/up: gate, up; down: row tiles 0 and 1
-        tc_ld16(tb + c0, g);
-        tc_ld16(tb + 128 + c0, u);
-        tc_ld_wait();
+      if (qw * 32 < jb.nn) {  // warp-uniform: a warp with no token of the job reads nothing
+        const uint32_t tb = tmem + ((uint32_t)(qw * 32) << 16) + ab * 256;
+        bool range_ok = true;
+        uint16_t* hp = a.h + s * a.Imax + jb.mt * kBM;
+#pragma unroll 1
+        for (int c0 = half * (kBM / 2); c0 < (half + 1) * (kBM / 2); c0 += 16) {
+          uint32_t g[16], u[16];
+          tc_ld16(tb + c0, g);
+          tc_ld16(tb + kBM + c0, u);
+          tc_ld_wait();
+          uint32_t hv2[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int n = c0 + i;
-          if (n < jb.nn) {
-            const size_t s = (size_t)jb.off + jb.n0 + n;
-            if (GU) {  // undo the token's power-of-two prescale of x (exact)
-              const float xs = colf[n];
-              const float gv = __uint_as_float(g[i]) * xs, uv = __uint_as_float(u[i]) * xs;
-              const float hv = gv / (1.0f + expf(-gv)) * uv;
-              range_ok = range_ok && fabsf(hv) < 65504.f;
-              a.h[s * a.Imax + jb.mt * kBM + row] = __half_as_ushort(__float2half_rn(hv));
-            } else {
-              float* pp = a.partial + s * a.H + jb.mt * (2 * kBM) + row;
-              pp[0] = colf[n] * __uint_as_float(g[i]);
-              pp[kBM] = colf[n] * __uint_as_float(u[i]);
+          for (int i = 0; i < 8; ++i) {
+            float hv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {  // undo the token's power-of-two prescale of x (exact)
+              const float gv = __uint_as_float(g[2 * i + e]) * cf, uv = __uint_as_float(u[2 * i + e]) * cf;
+              hv[e] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;  // rounded to fp16 below
+              range_ok = range_ok && (!valid || fabsf(hv[e]) < 65504.f);
             }
+            const __half2 h2 = __floats2half2_rn(hv[0], hv[1]);
+            hv2[i] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(hp + c0);
+            d4[0] = make_uint4(hv2[0], hv2[1], hv2[2], hv2[3]);
+            d4[1] = make_uint4(hv2[4], hv2[5], hv2[6], hv2[7]);
           }
         }
+        if (!range_ok) atomicOr(a.status, DEV_RANGE);
       }
-      if (!range_ok) atomicOr(a.status, DEV_RANGE);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty + 8 * ab);
+    }
+    } else {
+    // Down: thread = one output row of weight tile `half` (TMEM lane), the
+    // columns are the job's tokens; each warp store is a contiguous 128-byte
+    // segment of one token's partial row.
+    const int row = qw * 32 + lane;
+    for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
+      const Job jb = job_of(j);
+      const int ab = jcnt & 1;
+      // the routing weights of the job's pairs, fetched while its MMAs run
+      float* colf = s_colf[ab];
+      const int e = half * kBM + row;
+      if (e < jb.nn) colf[e] = jb.sh ? 1.0f : __ldg(a.w + a.sorted_pair[jb.off + jb.n0 + e]);
+      named_bar_sync(1, 32 * kEpiWarps);
+      if (!__all_sync(0xffffffffu, mbar_wait_short(acc_full + 8 * ab, (jcnt >> 1) & 1, a.status))) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem + ((uint32_t)(qw * 32) << 16) + ab * 256 + half * kBM;
+      float* pcol = a.partial + (size_t)(jb.off + jb.n0) * a.H + jb.mt * (2 * kBM) + half * kBM + row;
+      for (int c0 = 0; c0 < jb.np; c0 += 16) {
+        uint32_t v[16];
+        tc_ld16(tb + c0, v);
+        tc_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (c0 + i < jb.nn) pcol[(size_t)(c0 + i) * a.H] = colf[c0 + i] * __uint_as_float(v[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty + 8 * ab);
+    }
     }
   }
   tc_fence_before();
