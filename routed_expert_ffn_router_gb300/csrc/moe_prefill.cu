@@ -383,7 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
         }
         tc_commit_el(a_empty + 8 * as, lead);  // the tiles are free once these MMAs are done
         ++acnt;
-        if (++u == spb) {
+        // a slot is free after its last step; a job's last slot may hold fewer
+        // than spb steps (K / 64 not a multiple of spb)
+        if (++u == spb || kb == nkb - 1) {
           tc_commit_el(b_empty + 8 * bs, lead);
           ++bcnt;
           u = 0;

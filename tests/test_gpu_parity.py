@@ -286,6 +286,18 @@ def test_ragged_windows(T):
     check_y(out["y"], y, what=f"T={T}")
 
 
+def test_prefill_k_not_a_multiple_of_slot_steps():
+    """Prefill GEMMs with K = 768 in both (12 steps of 64 columns, where a token slot holds 8
+    steps for jobs of up to 16 tokens) and two or three jobs per CTA: each job's last, partly
+    used token slot must be released before the next job of the CTA reads the ring."""
+    cfg = synth.MoeConfig("k768", H=768, I=768, E=64, k=4, T=384, shared_I=768, zipf_s=1.0)
+    inp = synth.make_layer(cfg, 5)
+    out, _ = run_layer(inp)
+    ids, w, we, y = oracle_layer(inp, inp.logits.numpy())
+    assert np.array_equal(out["ids"], ids)
+    check_y(out["y"], y, what="K = 768 prefill")
+
+
 def test_min_shapes_and_max_k():
     cfg = synth.MoeConfig("min", H=128, I=128, E=40, k=32, T=3, shared_I=128, zipf_s=0.0)
     inp = synth.make_layer(cfg, 2)
