@@ -256,6 +256,27 @@ def test_expert_cache_random_slot_map_and_misses():
     check_y(out["y"], y, what="random slot map")
 
 
+def test_prefill_random_slot_map_and_misses():
+    """Prefill path (64 tokens: the tcgen05 GEMMs) through a slot map with 60% of the experts
+    resident and a shared expert: the miss list equals the oracle's permutation, and y sums the
+    resident experts and the shared one."""
+    cfg = synth.MoeConfig("pf_ec", H=1024, I=512, E=64, k=8, T=64, shared_I=512, zipf_s=1.2)
+    inp = synth.make_layer(cfg, 6)
+    smt, S = synth.random_slot_map(cfg.E, 0.6, seed=11)
+    keep = (smt >= 0).nonzero().flatten()
+    for kname in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s"):
+        setattr(inp, kname, getattr(inp, kname)[keep].contiguous())
+    inp.S = S
+    inp.slot_map = smt
+    out, _ = run_layer(inp)
+    ids, w, we, y = oracle_layer(inp, inp.logits.numpy())
+    pm = oracle.permute(ids, cfg.E, smt.numpy())
+    assert pm["n_miss"] > 0
+    assert out["n_miss"][0] == pm["n_miss"]
+    assert np.array_equal(out["miss_ids"][:pm["n_miss"]], pm["miss_ids"])
+    check_y(out["y"], y, what="prefill, random slot map")
+
+
 def test_prefill_sampled_rows():
     """2,048-token chunk: every output row is finite; the oracle checks sampled
     rows, including rows routed to the hottest expert, the first and the last."""
