@@ -196,6 +196,85 @@ moe_status moe_profile_forget(void);
 moe_status moe_profile_totals(int32_t kind, double *total_ms, int64_t *count);
 const char *moe_profile_kind_name(int32_t kind);
 
+/* ---- Adaptive expert cache (host side) ----
+ * "extended-strata-moe reference", "The adaptive cache": which experts occupy
+ * a layer's pool slots is decided from the routing while decoding. A heat per
+ * (layer, expert) counts one pick per expert and window (windows of more than
+ * max_window_tokens rows do not count) and fades with a half-life in generated
+ * tokens. Every fill_every_tokens, free slots take the hottest experts not held
+ * (at most max_fills); every round_every_tokens, in a layer without free slots
+ * the i-th hottest expert not held replaces the i-th coldest held one while
+ * heat_in - in_picks > in_ratio * heat_out (at most max_swaps per round over
+ * all layers, the hottest incoming first). Layers holding every expert are
+ * left alone. The page's values: half-life 350 tokens, rounds every 32 tokens
+ * with 64 swaps, fills every 8 tokens with 128, ratio 1.5 plus 2 picks, windows
+ * of up to 32 tokens.
+ *
+ * The planner is host code on a HOST state buffer the caller owns (size from
+ * moe_cache_state_bytes, 8-byte aligned); it only decides and keeps each
+ * layer's slot map (int32 [E], -1 = not held, the moe_permute/moe_expert_ffn
+ * slot_map). For each returned move the caller copies expert `expert_in`'s
+ * codes and scales into pool slot `slot` of `layer` and uploads the layer's
+ * slot map before the next window reads the pool. Calls on one state must not
+ * run concurrently. Errors: MOE_ERR_INVALID (bad argument or not a state),
+ * MOE_ERR_WORKSPACE (state buffer too small or misaligned); the int32/int64
+ * returning calls give -1. */
+typedef struct {
+  int32_t n_layers, n_experts;     /* 1 .. 65536 each */
+  double half_life_tokens;         /* > 0 */
+  int32_t round_every_tokens;      /* >= 1 */
+  int32_t max_swaps;               /* >= 0 */
+  int32_t fill_every_tokens;       /* >= 1 */
+  int32_t max_fills;               /* >= 0 */
+  double in_ratio;                 /* >= 0 */
+  double in_picks;
+  int32_t max_window_tokens;       /* >= 1 */
+  int32_t reserved;
+} moe_cache_params;
+
+/* One move of a round: expert_in takes slot `slot` of `layer`; expert_out is
+ * the expert it evicts, -1 when the slot was free. */
+typedef struct {
+  int32_t layer, slot, expert_in, expert_out;
+} moe_cache_swap;
+
+/* Bytes of a state for these params and slots[n_layers] (HOST array, pool
+ * slots per layer); 0 for invalid arguments. */
+size_t moe_cache_state_bytes(const moe_cache_params *p, const int32_t *slots);
+/* Initialise a state: every slot free, heat 0, clock 0. */
+moe_status moe_cache_init(void *state, size_t bytes, const moe_cache_params *p, const int32_t *slots);
+/* Place experts[0..n) (HOST, distinct) into slots 0..n-1 of a layer, freeing
+ * the rest (e.g. a hottest-first start, or a layer held whole). */
+moe_status moe_cache_set_resident(void *state, int32_t layer, const int32_t *experts, int32_t n);
+/* Count one window's routing of a layer: ids (HOST int32 [T][k], e.g. moe_route's
+ * output copied back) add one pick to every distinct expert. */
+moe_status moe_cache_observe(void *state, int32_t layer, const int32_t *ids, int32_t T, int32_t k);
+/* Advance the clock by n_tokens generated tokens after a window: heats fade by
+ * 2^(-n_tokens / half_life), then the fill round and the swap round run if
+ * their clock has come (once each, fills first). swaps (HOST) receives the
+ * moves; n_max must be at least max_fills + max_swaps. Returns the number of
+ * moves. */
+int32_t moe_cache_advance(void *state, int32_t n_tokens, moe_cache_swap *swaps, int32_t n_max);
+/* A swap round now with at most max_swaps moves (n_max >= max_swaps), for
+ * callers that decode in chunks. Returns the number of moves. */
+int32_t moe_cache_rebalance(void *state, int32_t max_swaps, moe_cache_swap *swaps, int32_t n_max);
+/* Copy out a layer's slot map (HOST int32 [E]) or its heats (HOST double [E]). */
+moe_status moe_cache_slot_map(const void *state, int32_t layer, int32_t *slot_map);
+moe_status moe_cache_heat(const void *state, int32_t layer, double *heat);
+/* Experts brought into slots so far (fills and swaps). */
+int64_t moe_cache_swapped_total(const void *state);
+
+/* Expert profile ("Profile format (STRP)"), little-endian: "STRP", u32 version
+ * 1, u32 n_layers, u32 n_expert, u32 slots (all layers), u32 n_ranked, then
+ * n_ranked x (u16 layer, u16 expert) hottest first, then n_layers x n_expert x
+ * i32 rank (-1 unranked). Write: the pairs with heat > 0, by heat, then layer,
+ * then expert, into buf (HOST); n_max = 0 returns the size; returns the bytes
+ * written or -1. Load: validates magic, version, dimensions against the state,
+ * n_ranked and every pair, then fills each layer's slots with its pairs in
+ * profile order (a repeated pair is skipped); the rank table is not read. */
+int64_t moe_cache_profile_write(const void *state, uint8_t *buf, int64_t n_max);
+moe_status moe_cache_profile_load(void *state, const uint8_t *buf, int64_t n);
+
 #ifdef __cplusplus
 }
 #endif

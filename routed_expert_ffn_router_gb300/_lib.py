@@ -23,7 +23,10 @@ EXPORTS = ("moe_router_logits", "moe_route", "moe_permute", "moe_expert_ffn", "m
            "moe_workspace_bytes", "moe_workspace_init", "moe_read_status", "moe_status_str",
            "moe_last_launch_count", "moe_profile_enable", "moe_profile_collect",
            "moe_profile_forget", "moe_profile_totals", "moe_profile_kind_name",
-           "moe_expert_ffn_static")
+           "moe_expert_ffn_static", "moe_cache_state_bytes", "moe_cache_init",
+           "moe_cache_set_resident", "moe_cache_observe", "moe_cache_advance",
+           "moe_cache_rebalance", "moe_cache_slot_map", "moe_cache_heat",
+           "moe_cache_swapped_total", "moe_cache_profile_write", "moe_cache_profile_load")
 
 
 class MoeError(RuntimeError):
@@ -42,6 +45,20 @@ class moe_layer_desc(ctypes.Structure):
                 ("gate", moe_qmat), ("up", moe_qmat), ("down", moe_qmat),
                 ("shared_I", ctypes.c_int32),
                 ("shared_gate", moe_qmat), ("shared_up", moe_qmat), ("shared_down", moe_qmat)]
+
+
+class moe_cache_params(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("half_life_tokens", ctypes.c_double),
+                ("round_every_tokens", ctypes.c_int32), ("max_swaps", ctypes.c_int32),
+                ("fill_every_tokens", ctypes.c_int32), ("max_fills", ctypes.c_int32),
+                ("in_ratio", ctypes.c_double), ("in_picks", ctypes.c_double),
+                ("max_window_tokens", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class moe_cache_swap(ctypes.Structure):
+    _fields_ = [("layer", ctypes.c_int32), ("slot", ctypes.c_int32),
+                ("expert_in", ctypes.c_int32), ("expert_out", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -78,6 +95,17 @@ def load(path: str = LIB_PATH):
                                     ctypes.POINTER(ctypes.c_int64)], i32),
             "moe_profile_kind_name": ([ctypes.c_int32], ctypes.c_char_p),
             "moe_expert_ffn_static": ([D, P, i32, i32, P, P, P, P, P, P, P], i32),
+            "moe_cache_state_bytes": ([ctypes.POINTER(moe_cache_params), P], sz),
+            "moe_cache_init": ([P, sz, ctypes.POINTER(moe_cache_params), P], i32),
+            "moe_cache_set_resident": ([P, ctypes.c_int32, P, ctypes.c_int32], i32),
+            "moe_cache_observe": ([P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32], i32),
+            "moe_cache_advance": ([P, ctypes.c_int32, P, ctypes.c_int32], ctypes.c_int32),
+            "moe_cache_rebalance": ([P, ctypes.c_int32, P, ctypes.c_int32], ctypes.c_int32),
+            "moe_cache_slot_map": ([P, ctypes.c_int32, P], i32),
+            "moe_cache_heat": ([P, ctypes.c_int32, P], i32),
+            "moe_cache_swapped_total": ([P], ctypes.c_int64),
+            "moe_cache_profile_write": ([P, P, ctypes.c_int64], ctypes.c_int64),
+            "moe_cache_profile_load": ([P, P, ctypes.c_int64], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
