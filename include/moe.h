@@ -275,6 +275,23 @@ int64_t moe_cache_swapped_total(const void *state);
 int64_t moe_cache_profile_write(const void *state, uint8_t *buf, int64_t n_max);
 moe_status moe_cache_profile_load(void *state, const uint8_t *buf, int64_t n);
 
+/* ---- Routing traces (host side) ----
+ * "extended-strata-moe reference", "Routing trace format": one record per
+ * token and layer, little-endian: int32 layer, int32 k, k x int32 expert id,
+ * k x float32 weight.
+ * moe_trace_write: records of one layer's T tokens from HOST ids/w [T][k] (w
+ *   nullable: weights written as 0) into buf (HOST); n_max = 0 returns the
+ *   size; returns the bytes written, or -1 (bad argument, buffer too small).
+ * moe_trace_read: parses a buffer of records (any layers, any k <= k_max);
+ *   n_max = 0 counts them; else fills layer[r], k_out[r], ids[r][k_max] and
+ *   w[r][k_max] (HOST; slots past a record's k get id -1 and weight 0) for up
+ *   to n_max records. Returns the number of records, or -1 for a truncated or
+ *   malformed buffer (k < 1 or k > k_max) or more than n_max records. */
+int64_t moe_trace_write(int32_t layer, const int32_t *ids, const float *w, int32_t T, int32_t k,
+                        uint8_t *buf, int64_t n_max);
+int64_t moe_trace_read(const uint8_t *buf, int64_t n, int32_t *layer, int32_t *k_out, int32_t *ids,
+                       float *w, int32_t k_max, int64_t n_max);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,8 @@ EXPORTS = ("moe_router_logits", "moe_route", "moe_permute", "moe_expert_ffn", "m
            "moe_expert_ffn_static", "moe_cache_state_bytes", "moe_cache_init",
            "moe_cache_set_resident", "moe_cache_observe", "moe_cache_advance",
            "moe_cache_rebalance", "moe_cache_slot_map", "moe_cache_heat",
-           "moe_cache_swapped_total", "moe_cache_profile_write", "moe_cache_profile_load")
+           "moe_cache_swapped_total", "moe_cache_profile_write", "moe_cache_profile_load",
+           "moe_trace_write", "moe_trace_read")
 
 
 class MoeError(RuntimeError):
@@ -106,6 +107,9 @@ def load(path: str = LIB_PATH):
             "moe_cache_swapped_total": ([P], ctypes.c_int64),
             "moe_cache_profile_write": ([P, P, ctypes.c_int64], ctypes.c_int64),
             "moe_cache_profile_load": ([P, P, ctypes.c_int64], i32),
+            "moe_trace_write": ([ctypes.c_int32, P, P, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int64],
+                                ctypes.c_int64),
+            "moe_trace_read": ([P, ctypes.c_int64, P, P, P, P, ctypes.c_int32, ctypes.c_int64], ctypes.c_int64),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
