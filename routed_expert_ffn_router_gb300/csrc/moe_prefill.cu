@@ -52,8 +52,8 @@
 namespace moe {
 namespace pf {
 
-constexpr int kBM = 128;              // weight rows per job (M of the MMA)
-constexpr int kNT = 128;              // tokens per job at most (N of the MMA)
+constexpr int kBM = 128;              // weight rows per tile (two tiles per job)
+constexpr int kNT = 128;              // tokens per job at most (gate/up: the MMA's M; down: its N)
 constexpr int kRawSt = 2, kASt = 2, kBSt = 4;
 // warps 0-3 and 15-18 epilogue, 4-11 and 19-26 dequant, 12-13 producers, 14 MMA
 constexpr int kThreads = 864;
@@ -158,7 +158,7 @@ __device__ __forceinline__ void dequant_word_h(uint32_t wd, __half2 s2, uint32_t
 
 struct Job {
   int a, mt, n0, nn, np;   // active entry, row tile, first token slot, tokens, tokens rounded to 16
-  int bsel;                // B box of 16 << bsel rows; a B slot holds 8 >> bsel boxes
+  int bsel;                // token box of 16 << bsel rows; a token slot holds 8 >> bsel boxes
   int off, slot;           // first sorted row of the expert; pool slot (-1: shared)
   bool sh;
 };
