@@ -248,6 +248,26 @@ def test_sparse_equals_dense_then_mask(name):
     assert np.max(np.abs(y - ref)) <= 1e-12 * np.max(np.abs(ref))
 
 
+def test_negative_control_one_corrupted_byte_fails_the_tolerance_gate():
+    """Negative control (the pages prove a gate can go red by corrupting one byte):
+    one bit of one byte of an fp16 scale in a routed expert's down matrix moves y
+    far beyond the parity tolerance (2e-3 of max|y|) against the intact layer, while
+    the brute-force check of the corrupted layer still holds (so the gate compares
+    bytes, not the oracle with itself)."""
+    cfg = synth.MoeConfig("nc", H=256, I=128, E=8, k=2, T=4, shared_I=128, zipf_s=1.0)
+    inp = synth.make_layer(cfg, 3)
+    ids, w, _ = oracle.route(inp.logits.numpy(), cfg.k)
+    y = oracle.Layer(inp).rows(ids, w)
+    bad = synth.clone_pool(inp)
+    e = int(ids[0][0])
+    b = bad.down_s.view(torch.uint8).view(cfg.E, cfg.H, cfg.I // 32, 2)
+    b[e, 0, 0, 1] ^= 0x40                      # the high byte: the exponent's top bit
+    y_bad = oracle.Layer(bad).rows(ids, w)
+    assert np.abs(y_bad - y).max() > 2e-3 * np.abs(y).max()
+    ref_bad = _pins.dense_then_mask(bad, ids, w)
+    assert np.max(np.abs(y_bad - ref_bad)) <= 1e-12 * np.max(np.abs(ref_bad))
+
+
 @pytest.mark.slow
 def test_sparse_equals_dense_then_mask_decode_window_full():
     """Same brute-force check at the full decode-window size (H 2048, 128 experts)."""
