@@ -249,6 +249,9 @@ moe_status moe_cache_set_resident(void *state, int32_t layer, const int32_t *exp
 /* Count one window's routing of a layer: ids (HOST int32 [T][k], e.g. moe_route's
  * output copied back) add one pick to every distinct expert. */
 moe_status moe_cache_observe(void *state, int32_t layer, const int32_t *ids, int32_t T, int32_t k);
+/* The same for every layer of a window at once: ids (HOST int32 [n_layers][T][k]).
+ * Every id is validated before any layer is counted. */
+moe_status moe_cache_observe_layers(void *state, const int32_t *ids, int32_t T, int32_t k);
 /* Advance the clock by n_tokens generated tokens after a window: heats fade by
  * 2^(-n_tokens / half_life), then the fill round and the swap round run if
  * their clock has come (once each, fills first). swaps (HOST) receives the

@@ -24,7 +24,8 @@ EXPORTS = ("moe_router_logits", "moe_route", "moe_permute", "moe_expert_ffn", "m
            "moe_last_launch_count", "moe_profile_enable", "moe_profile_collect",
            "moe_profile_forget", "moe_profile_totals", "moe_profile_kind_name",
            "moe_expert_ffn_static", "moe_cache_state_bytes", "moe_cache_init",
-           "moe_cache_set_resident", "moe_cache_observe", "moe_cache_advance",
+           "moe_cache_set_resident", "moe_cache_observe", "moe_cache_observe_layers",
+           "moe_cache_advance",
            "moe_cache_rebalance", "moe_cache_slot_map", "moe_cache_heat",
            "moe_cache_swapped_total", "moe_cache_profile_write", "moe_cache_profile_load",
            "moe_trace_write", "moe_trace_read")
@@ -100,6 +101,7 @@ def load(path: str = LIB_PATH):
             "moe_cache_init": ([P, sz, ctypes.POINTER(moe_cache_params), P], i32),
             "moe_cache_set_resident": ([P, ctypes.c_int32, P, ctypes.c_int32], i32),
             "moe_cache_observe": ([P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32], i32),
+            "moe_cache_observe_layers": ([P, P, ctypes.c_int32, ctypes.c_int32], i32),
             "moe_cache_advance": ([P, ctypes.c_int32, P, ctypes.c_int32], ctypes.c_int32),
             "moe_cache_rebalance": ([P, ctypes.c_int32, P, ctypes.c_int32], ctypes.c_int32),
             "moe_cache_slot_map": ([P, ctypes.c_int32, P], i32),

@@ -58,6 +58,15 @@ class ExpertCache:
         T, k = a.shape
         _lib._check("moe_cache_observe", self.L.moe_cache_observe(self._st(), layer, a.ctypes.data, T, k))
 
+    def observe_layers(self, ids):
+        """One window's routing ids [n_layers][T][k] (host) of every layer."""
+        a = np.ascontiguousarray(np.asarray(ids, np.int32))
+        Ln, T, k = a.shape
+        if Ln != self.p.n_layers:
+            raise ValueError("ids must hold every layer")
+        _lib._check("moe_cache_observe_layers",
+                    self.L.moe_cache_observe_layers(self._st(), a.ctypes.data, T, k))
+
     def _out(self, n):
         if n < 0:
             raise _lib.MoeError("moe_cache", _lib.MOE_ERR_INVALID, "invalid argument")
@@ -98,3 +107,19 @@ class ExpertCache:
     def load_profile(self, data: bytes):
         buf = (ctypes.c_uint8 * len(data)).from_buffer_copy(data)
         _lib._check("moe_cache_profile_load", self.L.moe_cache_profile_load(self._st(), buf, len(data)))
+
+
+POOL_TENSORS = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
+
+
+def copy_moves(pool, store, moves, layer=0):
+    """Apply a round's moves of one layer: expert `expert_in`'s codes and scales
+    from `store` (any object with the six [E][...] tensors gate_q ... down_s, e.g.
+    pinned host memory) into slot `slot` of `pool` (the same six tensors with S
+    slots, e.g. the device pool a layer reads). Copies are issued on the
+    current stream; call between windows, then upload the layer's slot map."""
+    for m_layer, slot, e_in, _ in moves:
+        if m_layer != layer:
+            continue
+        for name in POOL_TENSORS:
+            getattr(pool, name)[slot].copy_(getattr(store, name)[e_in], non_blocking=True)

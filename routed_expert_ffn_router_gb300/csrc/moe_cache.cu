@@ -333,6 +333,21 @@ moe_status moe_cache_observe(void* state, int32_t layer, const int32_t* ids, int
   return MOE_OK;
 }
 
+moe_status moe_cache_observe_layers(void* state, const int32_t* ids, int32_t T, int32_t k) {
+  View v;
+  if (!view_of(state, &v)) return MOE_ERR_INVALID;
+  if (T < 0 || k < 1 || (T > 0 && !ids)) return MOE_ERR_INVALID;
+  const size_t P = (size_t)T * k, E = (size_t)v.h->p.n_experts;
+  const size_t all = P * (size_t)v.h->p.n_layers;
+  for (size_t i = 0; i < all; ++i)  // validate every layer before counting any
+    if (ids[i] < 0 || (size_t)ids[i] >= E) return MOE_ERR_INVALID;
+  for (int l = 0; l < v.h->p.n_layers; ++l) {
+    const moe_status s = moe_cache_observe(state, l, ids + (size_t)l * P, T, k);
+    if (s != MOE_OK) return s;
+  }
+  return MOE_OK;
+}
+
 int32_t moe_cache_advance(void* state, int32_t n_tokens, moe_cache_swap* swaps, int32_t n_max) {
   View v;
   if (!view_of(state, &v) || n_tokens < 0) return -1;

@@ -247,3 +247,48 @@ def test_matches_oracle_on_random_traces(seed):
     assert c.swapped_total() == o.swapped
     assert n_fill > 10 and n_swap > 10          # both kinds of round did work
     assert c.profile_bytes() == o.profile_bytes()
+
+
+def test_observe_layers_equals_per_layer_calls():
+    rng = np.random.default_rng(5)
+    L, E, T, k = 3, 16, 6, 2
+    a, b = ExpertCache(L, E, [4, 4, 4]), ExpertCache(L, E, [4, 4, 4])
+    for _ in range(5):
+        ids = np.stack([np.stack([rng.choice(E, k, replace=False) for _ in range(T)]) for _ in range(L)])
+        a.observe_layers(ids)
+        for l in range(L):
+            b.observe(l, ids[l])
+        assert a.advance(4) == b.advance(4)
+    for l in range(L):
+        assert list(a.heat(l)) == list(b.heat(l))
+    bad = np.zeros((L, T, k), np.int32)
+    bad[2, 0, 0] = E                         # out of range in the last layer
+    before = [a.heat(l).copy() for l in range(L)]
+    with pytest.raises(_lib.MoeError):
+        a.observe_layers(bad)
+    assert all(np.array_equal(a.heat(l), before[l]) for l in range(L))   # nothing counted
+
+
+def test_copy_moves_fills_the_pool_slots():
+    import torch
+    from routed_expert_ffn_router_gb300 import synth
+    from routed_expert_ffn_router_gb300.cache import POOL_TENSORS, copy_moves
+    cfg = synth.MoeConfig("cm", H=128, I=128, E=8, k=2, T=4, zipf_s=1.0)
+    store = synth.make_layer(cfg, 2)
+    S = 3
+
+    class Pool:
+        pass
+    pool = Pool()
+    for name in POOL_TENSORS:
+        t = getattr(store, name)
+        setattr(pool, name, torch.zeros((S,) + tuple(t.shape[1:]), dtype=t.dtype))
+    c = ExpertCache(1, cfg.E, [S])
+    for e in (6, 6, 1, 4, 4, 4):
+        window(c, 0, [[e]])
+    moves = c.advance(8)
+    assert [m[2] for m in moves] == [4, 6, 1]
+    copy_moves(pool, store, moves)
+    for _, slot, e_in, _ in moves:
+        for name in POOL_TENSORS:
+            assert torch.equal(getattr(pool, name)[slot], getattr(store, name)[e_in])
