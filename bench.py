@@ -311,6 +311,22 @@ class DecodeWindowWorkload:
         return {"gateup": gu, "down": dn}
 
 
+def dump_routing(path, outs, layer=0):
+    """With MOE_TRACE=<path>: write the routing of the bench's windows (their ids
+    and weights, one record per row in the routing-trace format of the Strata
+    pages) to <path>, for diffing runs. Returns the bytes written (0: no path)."""
+    if not path:
+        return 0
+    from routed_expert_ffn_router_gb300 import trace
+    n = 0
+    with open(path, "wb") as f:
+        for o in outs:
+            b = trace.encode(layer, o["ids"].cpu().numpy(), o["w"].cpu().numpy())
+            f.write(b)
+            n += len(b)
+    return n
+
+
 def capture(torch, fn, n, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -356,6 +372,8 @@ def run_ours(args, dist):
     wl.count_distinct(torch)
     code, bits = wl.layers[0].status()
     assert code == _lib.MOE_OK, f"device status {bits}"
+    if dist.rank == 0:
+        dump_routing(os.environ.get("MOE_TRACE"), wl.outs)
 
     # graphs of R consecutive steps; the i-th step of the whole run is step i
     R = divisor_le(K, 64)

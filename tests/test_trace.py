@@ -68,3 +68,20 @@ def test_write_argument_errors():
     assert L.moe_trace_write(0, None, None, 2, 2, None, 0) == -1                  # no ids
     buf = (np.zeros(10, np.uint8))
     assert L.moe_trace_write(0, ids.ctypes.data, None, 2, 2, buf.ctypes.data, 10) == -1  # too small
+
+
+def test_bench_routing_dump(tmp_path):
+    """bench.py's MOE_TRACE dump: the windows' routing as consecutive records."""
+    import torch
+    import bench
+    outs = [dict(ids=torch.tensor([[3, 1], [0, 2]], dtype=torch.int32),
+                 w=torch.tensor([[0.75, 0.25], [0.5, 0.5]])),
+            dict(ids=torch.tensor([[7, 6]], dtype=torch.int32), w=torch.tensor([[0.6, 0.4]]))]
+    assert bench.dump_routing(None, outs) == 0
+    path = tmp_path / "routing.bin"
+    n = bench.dump_routing(str(path), outs)
+    data = path.read_bytes()
+    assert n == len(data) == 3 * (8 + 16)
+    layer, k, ids, w = trace.decode(data, k_max=2)
+    assert ids.tolist() == [[3, 1], [0, 2], [7, 6]] and list(layer) == [0, 0, 0]
+    assert np.allclose(w, [[0.75, 0.25], [0.5, 0.5], [0.6, 0.4]])
