@@ -480,7 +480,111 @@ def run_ours(args, dist):
     return line
 
 
+def align_up(n: int, a: int) -> int:
+    return (n + a - 1) // a * a
+
+
+def carve(torch, buf, off, shape, dtype):
+    """A typed view of bytes [off, off + size) of a uint8 buffer."""
+    n = 1
+    for d in shape:
+        n *= d
+    es = torch.empty((), dtype=dtype).element_size()
+    assert off % es == 0 and off + n * es <= buf.numel()
+    return buf[off:off + n * es].view(dtype).view(*shape)
+
+
+def staged_io(torch, cfg, x_dtype, device):
+    """Buffers of the end-to-end step, one per direction, so that a step makes
+    one host-to-device copy of its inputs and one device-to-host copy of its
+    results (a caller's natural layout: each copy is a latency, whatever its
+    size). Inputs [logits f32 T x E | x T x H], x 256-byte aligned; outputs
+    [y f32 T x H | ids i32 T x k | w f32 T x k | n_miss i32 | miss_ids i32 E],
+    the first four read back. Returns (din, din views, dout, dout views,
+    input bytes, output bytes read back)."""
+    T, E, H, k = cfg.T, cfg.E, cfg.H, cfg.k
+    xe = torch.empty((), dtype=x_dtype).element_size()
+    o_x = align_up(T * E * 4, 256)
+    n_in = o_x + T * H * xe
+    din = torch.empty(n_in, dtype=torch.uint8, device=device)
+    vin = {"logits": carve(torch, din, 0, (T, E), torch.float32),
+           "x": carve(torch, din, o_x, (T, H), x_dtype)}
+    o_ids = T * H * 4
+    o_w = o_ids + T * k * 4
+    o_nm = o_w + T * k * 4
+    n_back = o_nm + 4
+    o_miss = align_up(n_back, 256)
+    dout = torch.empty(o_miss + E * 4, dtype=torch.uint8, device=device)
+    vout = {"y": carve(torch, dout, 0, (T, H), torch.float32),
+            "ids": carve(torch, dout, o_ids, (T, k), torch.int32),
+            "w": carve(torch, dout, o_w, (T, k), torch.float32),
+            "n_miss": carve(torch, dout, o_nm, (1,), torch.int32),
+            "miss_ids": carve(torch, dout, o_miss, (E,), torch.int32)}
+    return din, vin, dout, vout, n_in, n_back
+
+
 def run_e2e(torch, wl, stream, K, R, dist):
+    """End to end through the C ABI with host buffers: every step copies its
+    window's logits and activations from pinned host memory (one copy), runs
+    the layer, and copies y, ids, w and n_miss back (one copy). If that staging
+    fails its own check, the step is timed with one copy per tensor instead."""
+    try:
+        return run_e2e_staged(torch, wl, stream, K, R, dist)
+    except Exception as ex:  # the headline line must still print
+        torch.cuda.synchronize()
+        res = run_e2e_separate(torch, wl, stream, K, R, dist)
+        res["staging"] = f"one copy per tensor (staged copies failed: {type(ex).__name__}: {ex})"
+        return res
+
+
+def run_e2e_staged(torch, wl, stream, K, R, dist):
+    cfg = wl.cfg
+    nw = min(wl.n_windows, 16)
+    din, vin, dout, vout, n_in, n_back = staged_io(torch, cfg, wl.x[0].dtype, wl.x[0].device)
+    h_in = []
+    for w in range(nw):
+        h = torch.empty(n_in, dtype=torch.uint8).pin_memory()
+        carve(torch, h, 0, tuple(wl.logits[w].shape), torch.float32).copy_(wl.logits[w].cpu())
+        o_x = vin["x"].data_ptr() - din.data_ptr()
+        carve(torch, h, o_x, tuple(wl.x[w].shape), wl.x[w].dtype).copy_(wl.x[w].cpu())
+        h_in.append(h)
+    h_out = torch.empty(n_back, dtype=torch.uint8).pin_memory()
+    d_back = dout[:n_back]
+
+    def step(i):
+        din.copy_(h_in[i % nw], non_blocking=True)
+        wl.layers[i % wl.n_pools].forward(vin["logits"], vin["x"], out=vout, stream=stream)
+        h_out.copy_(d_back, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(4):
+            step(i)
+    torch.cuda.synchronize()
+    g = capture(torch, step, R, stream)
+    torch.cuda.synchronize()
+    time_graph(torch, [g], 2, stream)
+    dist.barrier()
+    torch.cuda.synchronize()
+    ms = time_graph(torch, [g], K // R, stream)
+    torch.cuda.synchronize()
+    # the last step's results came back whole and equal those of the device-timed run
+    last = (R - 1) % nw
+    y_back = carve(torch, h_out, 0, (cfg.T, cfg.H), torch.float32)
+    ids_back = carve(torch, h_out, vout["ids"].data_ptr() - dout.data_ptr(), (cfg.T, cfg.k),
+                     torch.int32)
+    good = (torch.equal(h_out, d_back.cpu()) and torch.equal(din.cpu(), h_in[last])
+            and torch.equal(y_back, wl.outs[last]["y"].cpu())
+            and torch.equal(ids_back, wl.outs[last]["ids"].cpu()))
+    if dist.max(0.0 if good else 1.0) > 0:  # every rank takes the same path
+        raise RuntimeError("staged end-to-end results differ from the device-timed run")
+    ms = dist.max(ms)
+    byts = dist.sum(sum(wl.step_bytes(i % nw) for r in range(K // R) for i in range(R)))
+    return {"value": round(byts / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "us_per_layer": round(ms / K * 1e3, 3), "h2d_bytes_per_step": n_in,
+            "d2h_bytes_per_step": n_back, "staging": "one copy per direction"}
+
+
+def run_e2e_separate(torch, wl, stream, K, R, dist):
     cfg = wl.cfg
     lay = wl.layers[0]
     nw = min(wl.n_windows, 16)
