@@ -106,3 +106,21 @@ def test_workspace_grows_with_T(lib):
         n = lib.moe_workspace_bytes(ctypes.byref(d), T)
         assert n >= prev and n % 256 == 0
         prev = n
+
+
+def test_static_entry_point_host_checks(lib):
+    # the fixed-scratch entry point refuses, before touching the device, a
+    # layer whose workspace exceeds its 16 MiB array, and reports bad
+    # descriptions like the workspace entry point does
+    big = _desc(H=2048, I=512, E=512, k=10, S=512, shared_I=512)
+    assert lib.moe_workspace_bytes(ctypes.byref(big), 2048) > (16 << 20)
+    assert lib.moe_expert_ffn_static(ctypes.byref(big), 4096, 1, 2048, 4096, 4096, None, 4096,
+                                     4096, 4096, None) == _lib.MOE_ERR_UNSUPPORTED
+    for kw, code in ((dict(E=0), _lib.MOE_ERR_INVALID), (dict(H=200), _lib.MOE_ERR_UNSUPPORTED),
+                     (dict(ptr=4097), _lib.MOE_ERR_INVALID)):
+        d = _desc(**kw)
+        assert lib.moe_expert_ffn_static(ctypes.byref(d), 4096, 1, 4, 4096, 4096, None, 4096,
+                                         4096, 4096, None) == code
+    d = _desc()
+    assert lib.moe_expert_ffn_static(ctypes.byref(d), 4096, 1, -1, 4096, 4096, None, 4096, 4096,
+                                     4096, None) == _lib.MOE_ERR_INVALID
