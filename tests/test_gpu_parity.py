@@ -470,3 +470,31 @@ def test_fused_flags_non_finite_logit():
     lay.clear_status()
     lay.forward(inp.logits, inp.x)
     assert lay.status()[0] == _lib.MOE_OK
+
+
+def test_negative_control_one_corrupted_byte_fails_the_gate():
+    """Negative control on the GPU path: one flipped bit (the exponent's top bit)
+    in one byte of an fp16 scale of a routed expert's down matrix. Against the
+    intact layer's oracle, the rows routed to that expert must then fail the
+    2e-3 gate, so the gate compares bytes and is not vacuous. The corrupted pool
+    must still match its own oracle, and the rows not routed to that expert must
+    be bitwise unchanged."""
+    cfg = synth.DECODE_WINDOW
+    inp = synth.make_layer(cfg, 0, device=DEV)
+    out, _ = run_layer(inp)
+    hinp = inp.to("cpu")
+    ids, w, we, y = oracle_layer(hinp, hinp.logits.numpy())
+    check_y(out["y"], y, what="intact")
+    e = int(ids[0][0])
+    bad = synth.clone_pool(inp)
+    b = bad.down_s.view(torch.uint8).view(cfg.E, cfg.H, cfg.I // 32, 2)
+    b[e, 0, 0, 1] ^= 0x40
+    out_bad, _ = run_layer(bad)
+    assert np.array_equal(out_bad["ids"], ids)
+    hit = [t for t in range(cfg.T) if e in ids[t]]
+    miss = [t for t in range(cfg.T) if e not in ids[t]]
+    dy = np.abs(out_bad["y"][hit].astype(np.float64) - y[hit]).max()
+    assert dy > TOL * np.abs(y).max(), dy
+    y_bad = oracle.Layer(bad.to("cpu")).rows(ids, w, rows=hit)
+    check_y(out_bad["y"][hit], y_bad, what="corrupted pool")
+    assert np.array_equal(out_bad["y"][miss], out["y"][miss])
