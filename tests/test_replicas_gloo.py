@@ -75,8 +75,20 @@ def test_reference_arm_under_two_ranks_prints_one_line():
            os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2", "--warmup", "1"]
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=280, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1, r.stdout[-2000:]
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 2
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    # the line carries every key of the bench contract, on the same metric and workload
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "e2e",
+                "cpu_baseline"):
+        assert key in d, key
+    import bench
+    assert d["metric"] == bench.METRIC and d["unit"] == "GB/s" and d["warmup"] >= 3
+    assert d["config"]["workload"].startswith("decode_window: 1 layer, T=8 rows")
+    assert d["e2e"]["value"] == d["value"] == d["cpu_baseline"]["value"] > 0
+    assert d["cpu_baseline"]["cores"] == 1 and d["vs_baseline"] is None
