@@ -41,7 +41,13 @@
  *
  * Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32), H and I (and shared_I)
  * multiples of 128 and at most 16384, T >= 0 (T = 0 is a no-op that reports
- * zero misses), every q/scale pool, x and y 16-byte aligned.
+ * zero misses), every q/scale pool, x and y 16-byte aligned. Three paths run a
+ * layer: windows of T <= 16 rows with bf16 x, H a multiple of 512 up to 8192
+ * and I, shared_I multiples of 256 take the one-launch decode kernel; T > 16
+ * with bf16 x and H, I, shared_I multiples of 256 take the tensor-core
+ * prefill kernels; every other call takes the separate-kernel path, which
+ * holds a row block over all of H in shared memory and so takes H <= 11392
+ * (MOE_ERR_UNSUPPORTED beyond, before anything is launched).
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H

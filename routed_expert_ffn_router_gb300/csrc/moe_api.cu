@@ -107,6 +107,10 @@ WsLayout ws_layout(int E, int k, int T, int H, int I, int shI) {
 
 }  // namespace moe
 
+namespace moe {
+bool ffn_decode_supported(int H);  // moe_decode.cu: the separate-kernel path's H limit
+}  // namespace moe
+
 using namespace moe;
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -356,6 +360,8 @@ static moe_status expert_ffn_impl(const moe_layer_desc* Ld, const void* x, moe_d
   if (fused_decode_supported(Ld->H, Ld->I, Ld->shared_I, T, x_dtype == MOE_BF16))
     return fused_impl(Ld, nullptr, x, T, ids, w, slot_map, y, nullptr, nullptr, miss_ids, n_miss,
                       ws, L, st);
+  const bool tc = prefill_tc_supported(Ld->H, Ld->I, Ld->shared_I, T, x_dtype == MOE_BF16);
+  if (!tc && !ffn_decode_supported(Ld->H)) return MOE_ERR_UNSUPPORTED;
   const bool has_shared = Ld->shared_I > 0;
   PermuteOut o;
   o.offsets = at<int32_t>(ws, L.offsets);
@@ -399,7 +405,7 @@ static moe_status expert_ffn_impl(const moe_layer_desc* Ld, const void* x, moe_d
   a.partial = at<float>(ws, L.partial);
   a.y = y;
   a.status = o.status;
-  if (prefill_tc_supported(a.H, a.I, a.shI, T, x_dtype == MOE_BF16)) {
+  if (tc) {
     if ((e = launch_ffn_prefill_tc(a, x, st)) != cudaSuccess) return MOE_ERR_CUDA;
     return cuda_status(launch_combine(a, st));
   }
@@ -438,6 +444,9 @@ moe_status moe_layer_forward(const moe_layer_desc* L, const float* logits, const
     return fused_impl(L, logits, x, T, nullptr, nullptr, slot_map, y, ids, w, miss_ids, n_miss, ws,
                       Lw, st);
   }
+  if (!prefill_tc_supported(L->H, L->I, L->shared_I, T, x_dtype == MOE_BF16) &&
+      !ffn_decode_supported(L->H))
+    return MOE_ERR_UNSUPPORTED;
   cudaError_t e = launch_route(logits, T, L->E, L->k, ids, w, at<int32_t>(ws, Lw.status), st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   return expert_ffn_impl(L, x, x_dtype, T, ids, w, slot_map, y, miss_ids, n_miss, ws, ws_bytes, st);

@@ -446,6 +446,16 @@ static cudaError_t set_smem(const void* fn, size_t bytes) {
   return cudaSuccess;
 }
 
+// Whether the separate-kernel path takes hidden size H: its gate/up CTA holds 16
+// rows of gate and up codes over all of H with their scales and block
+// corrections (unit_smem<2>(H, H).total bytes, plus 128 bytes of static shared
+// memory) within the 227 KB of shared memory a CTA may opt into on sm_103a.
+// That is H <= 11,392 in multiples of 128; the down kernel's rows are I long
+// and fit for every I the library takes.
+bool ffn_decode_supported(int H) {
+  return unit_smem<2>(H, H).total + 128 <= (size_t)227 * 1024;
+}
+
 cudaError_t launch_ffn_decode(const FfnArgs& a, const void* x, bool x_bf16, int cu_max,
                               cudaStream_t st) {
   cudaError_t err;

@@ -124,3 +124,20 @@ def test_static_entry_point_host_checks(lib):
     d = _desc()
     assert lib.moe_expert_ffn_static(ctypes.byref(d), 4096, 1, -1, 4096, 4096, None, 4096, 4096,
                                      4096, None) == _lib.MOE_ERR_INVALID
+
+
+@pytest.mark.parametrize("entry", ["moe_expert_ffn", "moe_layer_forward"])
+def test_separate_path_h_limit_is_reported_before_any_launch(lib, entry):
+    # T <= 16 with H = 12288 (> 8192) cannot take the one-launch decode kernel
+    # and is no prefill chunk: the separate-kernel path would need more than
+    # 227 KB of shared memory per CTA, so the call is refused up front
+    d = _desc(H=12288, I=128, E=8, k=2, S=8)
+    need = lib.moe_workspace_bytes(ctypes.byref(d), 4)
+    assert need > 0
+    if entry == "moe_expert_ffn":
+        rc = lib.moe_expert_ffn(ctypes.byref(d), 4096, 1, 4, 4096, 4096, None, 4096, 4096, 4096,
+                                4096, need, None)
+    else:
+        rc = lib.moe_layer_forward(ctypes.byref(d), 4096, 4096, 1, 4, None, 4096, 4096, 4096, 4096,
+                                   4096, 4096, need, None)
+    assert rc == _lib.MOE_ERR_UNSUPPORTED
