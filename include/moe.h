@@ -46,8 +46,11 @@
  * and I, shared_I multiples of 256 take the one-launch decode kernel; T > 16
  * with bf16 x and H, I, shared_I multiples of 256 take the tensor-core
  * prefill kernels; every other call takes the separate-kernel path, which
- * holds a row block over all of H in shared memory and so takes H <= 11392
- * (MOE_ERR_UNSUPPORTED beyond, before anything is launched).
+ * holds a row block over all of H in shared memory and so takes H <= 11392.
+ * The prefill and separate paths take T <= 65535 rows, and the separate path
+ * at most 65535 work units (sum over experts of ceil(rows / 16), plus the
+ * shared expert's). Calls beyond these limits return MOE_ERR_UNSUPPORTED
+ * before anything is launched.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H

@@ -111,6 +111,19 @@ namespace moe {
 bool ffn_decode_supported(int H);  // moe_decode.cu: the separate-kernel path's H limit
 }  // namespace moe
 
+// Rows of a call, and work units of the separate-kernel path, index the second
+// grid dimension of some launches (combine, x staging, gate/up, down).
+constexpr int kMaxGridY = 65535;
+
+// Whether the launches other than the one-launch decode kernel take this call:
+// at most kMaxGridY rows, and on the separate-kernel path (not the tensor-core
+// prefill) an H whose row block fits shared memory and at most kMaxGridY units.
+static bool paths_take(const moe_layer_desc* Ld, int T, bool x_bf16, const moe::WsLayout& L) {
+  if (T > kMaxGridY) return false;
+  if (moe::prefill_tc_supported(Ld->H, Ld->I, Ld->shared_I, T, x_bf16)) return true;
+  return moe::ffn_decode_supported(Ld->H) && L.cu_max <= kMaxGridY;
+}
+
 using namespace moe;
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -360,8 +373,8 @@ static moe_status expert_ffn_impl(const moe_layer_desc* Ld, const void* x, moe_d
   if (fused_decode_supported(Ld->H, Ld->I, Ld->shared_I, T, x_dtype == MOE_BF16))
     return fused_impl(Ld, nullptr, x, T, ids, w, slot_map, y, nullptr, nullptr, miss_ids, n_miss,
                       ws, L, st);
+  if (!paths_take(Ld, T, x_dtype == MOE_BF16, L)) return MOE_ERR_UNSUPPORTED;
   const bool tc = prefill_tc_supported(Ld->H, Ld->I, Ld->shared_I, T, x_dtype == MOE_BF16);
-  if (!tc && !ffn_decode_supported(Ld->H)) return MOE_ERR_UNSUPPORTED;
   const bool has_shared = Ld->shared_I > 0;
   PermuteOut o;
   o.offsets = at<int32_t>(ws, L.offsets);
@@ -444,9 +457,7 @@ moe_status moe_layer_forward(const moe_layer_desc* L, const float* logits, const
     return fused_impl(L, logits, x, T, nullptr, nullptr, slot_map, y, ids, w, miss_ids, n_miss, ws,
                       Lw, st);
   }
-  if (!prefill_tc_supported(L->H, L->I, L->shared_I, T, x_dtype == MOE_BF16) &&
-      !ffn_decode_supported(L->H))
-    return MOE_ERR_UNSUPPORTED;
+  if (!paths_take(L, T, x_dtype == MOE_BF16, Lw)) return MOE_ERR_UNSUPPORTED;
   cudaError_t e = launch_route(logits, T, L->E, L->k, ids, w, at<int32_t>(ws, Lw.status), st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   return expert_ffn_impl(L, x, x_dtype, T, ids, w, slot_map, y, miss_ids, n_miss, ws, ws_bytes, st);

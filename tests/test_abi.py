@@ -141,3 +141,21 @@ def test_separate_path_h_limit_is_reported_before_any_launch(lib, entry):
         rc = lib.moe_layer_forward(ctypes.byref(d), 4096, 4096, 1, 4, None, 4096, 4096, 4096, 4096,
                                    4096, 4096, need, None)
     assert rc == _lib.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("entry", ["moe_expert_ffn", "moe_layer_forward"])
+@pytest.mark.parametrize("kw,T,dtype", [
+    (dict(), 70000, 1),                                    # rows beyond a grid dimension
+    (dict(E=1024, k=32, S=1024), 65535, 0),                # fp32 x: too many 16-row work units
+])
+def test_row_and_unit_limits_are_reported_before_any_launch(lib, entry, kw, T, dtype):
+    d = _desc(**kw)
+    need = lib.moe_workspace_bytes(ctypes.byref(d), T)
+    assert need > 0
+    if entry == "moe_expert_ffn":
+        rc = lib.moe_expert_ffn(ctypes.byref(d), 4096, dtype, T, 4096, 4096, None, 4096, 4096,
+                                4096, 4096, need, None)
+    else:
+        rc = lib.moe_layer_forward(ctypes.byref(d), 4096, 4096, dtype, T, None, 4096, 4096, 4096,
+                                   4096, 4096, 4096, need, None)
+    assert rc == _lib.MOE_ERR_UNSUPPORTED
