@@ -452,8 +452,8 @@ moe_status moe_layer_forward(const moe_layer_desc* L, const float* logits, const
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (T == 0) return cuda_status(cudaMemsetAsync(n_miss, 0, sizeof(int32_t), st));
   if (!logits || !ids || !w) return MOE_ERR_INVALID;
+  if (!x || !y || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID;
   if (fused_decode_supported(L->H, L->I, L->shared_I, T, x_dtype == MOE_BF16)) {
-    if (!x || !y || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID;
     return fused_impl(L, logits, x, T, nullptr, nullptr, slot_map, y, ids, w, miss_ids, n_miss, ws,
                       Lw, st);
   }

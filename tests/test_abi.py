@@ -159,3 +159,15 @@ def test_row_and_unit_limits_are_reported_before_any_launch(lib, entry, kw, T, d
         rc = lib.moe_layer_forward(ctypes.byref(d), 4096, 4096, dtype, T, None, 4096, 4096, 4096,
                                    4096, 4096, 4096, need, None)
     assert rc == _lib.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("T", [4, 20])
+def test_layer_forward_checks_x_and_y_before_routing(lib, T):
+    # a missing or misaligned activation or output is reported before the
+    # routing launch, on the decode and the chunk paths alike
+    d = _desc()
+    need = lib.moe_workspace_bytes(ctypes.byref(d), T)
+    for x, y in ((None, 4096), (4096, None), (4104, 4096), (4096, 4104)):
+        rc = lib.moe_layer_forward(ctypes.byref(d), 4096, x, 1, T, None, y, 4096, 4096, 4096, 4096,
+                                   4096, need, None)
+        assert rc == _lib.MOE_ERR_INVALID, (x, y)
