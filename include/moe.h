@@ -41,7 +41,8 @@
  *
  * Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32), H and I (and shared_I)
  * multiples of 128 and at most 16384, T >= 0 (T = 0 is a no-op that reports
- * zero misses), every q/scale pool, x and y 16-byte aligned. Three paths run a
+ * zero misses) with T*k <= 2^30 pairs (moe_workspace_bytes returns 0 beyond),
+ * every q/scale pool, x and y 16-byte aligned. Three paths run a
  * layer: windows of T <= 16 rows with bf16 x, H a multiple of 512 up to 8192
  * and I, shared_I multiples of 256 take the one-launch decode kernel; T > 16
  * with bf16 x and H, I, shared_I multiples of 256 take the tensor-core
@@ -97,7 +98,8 @@ typedef struct {
 /* Router logits of the tiny configuration: logits[t][e] = sum_h x[t][h]*wg[h][e]
  * accumulated in float64 and rounded once to fp32 (so identical inputs give
  * the oracle's bits except at an fp32 rounding midpoint).
- * x [T][H] in x_dtype, wg [H][E] fp32, logits [T][E] fp32. */
+ * x [T][H] in x_dtype, wg [H][E] fp32, logits [T][E] fp32; T*E < 2^31
+ * (MOE_ERR_UNSUPPORTED beyond). */
 moe_status moe_router_logits(const void *x, moe_dtype x_dtype, const float *wg, int T, int H,
                              int E, float *logits, void *stream);
 

@@ -1,5 +1,6 @@
 // C ABI of the routed-expert FFN library: argument validation, workspace
 // layout and kernel sequencing. Declared in include/moe.h.
+#include <climits>
 #include <cstdio>
 #include <mutex>
 #include <vector>
@@ -110,6 +111,10 @@ WsLayout ws_layout(int E, int k, int T, int H, int I, int shI) {
 namespace moe {
 bool ffn_decode_supported(int H);  // moe_decode.cu: the separate-kernel path's H limit
 }  // namespace moe
+
+// (token, expert) pairs of a call at most: pair indices and counts are int32.
+constexpr int64_t kMaxPairs = int64_t(1) << 30;
+static bool pairs_ok(int T, int k) { return T >= 0 && (int64_t)T * k <= kMaxPairs; }
 
 // Rows of a call, and work units of the separate-kernel path, index the second
 // grid dimension of some launches (combine, x staging, gate/up, down).
@@ -252,7 +257,7 @@ const char* moe_profile_kind_name(int32_t kind) {
 }
 
 size_t moe_workspace_bytes(const moe_layer_desc* L, int T) {
-  if (check_desc(L) != MOE_OK || T < 0) return 0;
+  if (check_desc(L) != MOE_OK || !pairs_ok(T, L->k)) return 0;
   return ws_layout(L->E, L->k, T, L->H, L->I, L->shared_I).total;
 }
 
@@ -281,6 +286,7 @@ moe_status moe_router_logits(const void* x, moe_dtype x_dtype, const float* wg, 
   g_launches = 0;
   if (T < 0 || H < 1 || E < 1) return MOE_ERR_INVALID;
   if (x_dtype != MOE_F32 && x_dtype != MOE_BF16) return MOE_ERR_INVALID;
+  if ((int64_t)T * E > INT32_MAX) return MOE_ERR_UNSUPPORTED;  // one thread per logit
   if (T == 0) return MOE_OK;
   if (!x || !wg || !logits) return MOE_ERR_INVALID;
   return cuda_status(launch_router_logits(x, x_dtype == MOE_BF16, wg, T, H, E, logits,
@@ -306,6 +312,7 @@ moe_status moe_permute(const int32_t* ids, int T, int E, int k, const int32_t* s
   moe_status s = check_dims(E, k);
   if (s != MOE_OK) return s;
   if (T < 0 || S < 1) return MOE_ERR_INVALID;
+  if (!pairs_ok(T, k)) return MOE_ERR_UNSUPPORTED;
   if (!offsets || !miss_ids || !n_miss) return MOE_ERR_INVALID;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the permutation needs no activation buffers: size its workspace for H = I = 128
@@ -433,6 +440,7 @@ moe_status moe_expert_ffn(const moe_layer_desc* L, const void* x, moe_dtype x_dt
   moe_status s = check_desc(L);
   if (s != MOE_OK) return s;
   if (T < 0 || (x_dtype != MOE_F32 && x_dtype != MOE_BF16)) return MOE_ERR_INVALID;
+  if (!pairs_ok(T, L->k)) return MOE_ERR_UNSUPPORTED;
   if (!miss_ids || !n_miss) return MOE_ERR_INVALID;
   return expert_ffn_impl(L, x, x_dtype, T, ids, w, slot_map, y, miss_ids, n_miss, ws, ws_bytes,
                          static_cast<cudaStream_t>(stream));
@@ -446,6 +454,7 @@ moe_status moe_layer_forward(const moe_layer_desc* L, const float* logits, const
   moe_status s = check_desc(L);
   if (s != MOE_OK) return s;
   if (T < 0 || (x_dtype != MOE_F32 && x_dtype != MOE_BF16)) return MOE_ERR_INVALID;
+  if (!pairs_ok(T, L->k)) return MOE_ERR_UNSUPPORTED;
   if (!miss_ids || !n_miss) return MOE_ERR_INVALID;
   const WsLayout Lw = ws_layout(L->E, L->k, T, L->H, L->I, L->shared_I);
   if ((s = check_ws(ws, ws_bytes, Lw.total)) != MOE_OK) return s;

@@ -171,3 +171,19 @@ def test_layer_forward_checks_x_and_y_before_routing(lib, T):
         rc = lib.moe_layer_forward(ctypes.byref(d), 4096, x, 1, T, None, y, 4096, 4096, 4096, 4096,
                                    4096, need, None)
         assert rc == _lib.MOE_ERR_INVALID, (x, y)
+
+
+def test_pair_and_logit_counts_beyond_int32_are_refused(lib):
+    T = 1 << 26  # T * k = 2^31 pairs at k = 32
+    d = _desc(E=64, k=32, S=64)
+    assert lib.moe_workspace_bytes(ctypes.byref(d), T) == 0
+    assert lib.moe_permute(4096, T, 64, 32, None, 64, 4096, 4096, 4096, 4096, 4096, 4096, 1 << 40,
+                           None) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_expert_ffn(ctypes.byref(d), 4096, 1, T, 4096, 4096, None, 4096, 4096, 4096,
+                              4096, 1 << 40, None) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_layer_forward(ctypes.byref(d), 4096, 4096, 1, T, None, 4096, 4096, 4096, 4096,
+                                 4096, 4096, 1 << 40, None) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_expert_ffn_static(ctypes.byref(d), 4096, 1, T, 4096, 4096, None, 4096, 4096,
+                                     4096, None) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_router_logits(4096, 0, 4096, 1 << 22, 128, 1024, 4096,
+                                 None) == _lib.MOE_ERR_UNSUPPORTED
