@@ -28,9 +28,10 @@
  *    caller owns every buffer; the library allocates no device memory.
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*,
  *    NULL = the legacy default stream) and never synchronise, except
- *    moe_read_status(). They may be captured into a CUDA graph. The first call
- *    of a kind on a device queries and sets kernel attributes and encodes
- *    tensor maps: make it once before capturing (a warm-up call).
+ *    moe_read_status(). moe_route, moe_permute, moe_expert_ffn and
+ *    moe_layer_forward may be captured into a CUDA graph; the first call of
+ *    each on a device queries and sets kernel attributes and encodes tensor
+ *    maps, so make one call before capturing (a warm-up call).
  *  - Argument errors found on the host return before anything is launched:
  *    MOE_ERR_INVALID (bad value or null pointer), MOE_ERR_UNSUPPORTED (a shape
  *    outside the limits below), MOE_ERR_WORKSPACE (workspace too small or not
