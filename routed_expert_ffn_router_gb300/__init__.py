@@ -2,18 +2,20 @@
 
 The compute lives in libmoe_gb300.so (C ABI: include/moe.h); this package
 holds its ctypes binding (`_lib`), a small device-buffer owner (`layer`), the
-build script (`build`) and the seeded synthetic input generator (`synth`).
+adaptive expert cache's planner binding (`cache`), the routing-trace codec
+binding (`trace`), the build script (`build`) and the seeded synthetic input
+generator (`synth`).
 """
 from . import synth  # noqa: F401
 
-__all__ = ["synth", "lib", "layer"]
+__all__ = ["synth", "lib", "layer", "cache", "trace"]
 
 
 def __getattr__(name):
     if name == "lib":
         from . import _lib
         return _lib
-    if name == "layer":
-        from . import layer
-        return layer
+    if name in ("layer", "cache", "trace"):
+        import importlib
+        return importlib.import_module(f".{name}", __name__)
     raise AttributeError(name)
