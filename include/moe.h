@@ -41,6 +41,12 @@
  *    workspace; kernels never trap. Read it with moe_read_status().
  *  - Results are deterministic: run to run, and for the decode path (T <= 16)
  *    a row's output does not depend on the other rows of the window.
+ *  - A workspace serves one call at a time: calls that share one must be
+ *    ordered (one stream, or events). The one-launch decode kernel runs one
+ *    CTA per SM and its CTAs wait for each other's results, so it expects the
+ *    whole GPU: a kernel running beside it on another stream can keep some of
+ *    its CTAs from starting, and then its waits expire (MOE_ERR_TIMEOUT from
+ *    moe_read_status; re-initialise the workspace and repeat the call).
  *
  * Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32), H and I (and shared_I)
  * multiples of 128 and at most 16384, T >= 0 (T = 0 is a no-op that reports
