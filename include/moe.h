@@ -178,7 +178,8 @@ moe_status moe_expert_ffn_static(const moe_layer_desc *L, const void *x, moe_dty
                                  float *y, int32_t *miss_ids, int32_t *n_miss, void *stream);
 
 /* Workspace bytes a call with this layer and T rows needs (256-byte aligned
- * base required). L is a HOST pointer. Returns 0 for an invalid desc. */
+ * base required); it also serves every call with fewer rows. L is a HOST
+ * pointer. Returns 0 for an invalid desc or T (T < 0 or T*k > 2^30). */
 size_t moe_workspace_bytes(const moe_layer_desc *L, int T);
 
 /* Zero a workspace's status word and counters: once after allocating it, and
