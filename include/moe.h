@@ -36,9 +36,15 @@
  *    MOE_ERR_INVALID (bad value or null pointer), MOE_ERR_UNSUPPORTED (a shape
  *    outside the limits below), MOE_ERR_WORKSPACE (workspace too small or not
  *    256-byte aligned). A failed launch returns MOE_ERR_CUDA.
- *  - Problems only the device can see (non-finite logit, slot out of range, an
- *    expired bounded wait) are OR-ed into the status word at the start of the
- *    workspace; kernels never trap. Read it with moe_read_status().
+ *  - Problems only the device can see are OR-ed into the status word at the
+ *    start of the workspace; kernels never trap. Read it with
+ *    moe_read_status(). Bits: 1 a non-finite router logit (that row's routing
+ *    is unspecified); 2 a slot_map entry >= S, or an expert id outside [0, E)
+ *    given to moe_expert_ffn (the entry is treated as not resident, the id is
+ *    clamped); 4 a bounded wait expired after about a second (the call's
+ *    results are incomplete); 8 an intermediate value beyond the fp16 range
+ *    (an expert's SwiGLU output |h| >= 65504; the affected rows are
+ *    unspecified).
  *  - Results are deterministic: run to run, and for the decode path (T <= 16)
  *    a row's output does not depend on the other rows of the window.
  *  - A workspace serves one call at a time: calls that share one must be
