@@ -348,6 +348,33 @@ def time_graph(torch, graphs, reps, stream):
     return s.elapsed_time(e)
 
 
+def profile_steps(torch, _lib, wl, stream, R, reps, n_graphs, launches_per_step):
+    """Replays graph r % n_graphs for r < reps (the timed sequence) with event
+    pairs around every kernel; returns ({kind: (ms, launches)}, step ids)."""
+    _lib.moe_profile_enable(R * launches_per_step + 64)
+    steps = []
+    for gi in range(n_graphs):
+        rs = [r for r in range(reps) if r % n_graphs == gi]
+        if not rs:
+            continue
+        _lib.moe_profile_forget()
+        g = capture(torch, lambda i, b=gi * R: wl.step(b + i, stream), R, stream)
+        with torch.cuda.stream(stream):
+            g.replay()  # warm-up, not collected
+        torch.cuda.synchronize()
+        for _ in rs:
+            with torch.cuda.stream(stream):
+                g.replay()
+            torch.cuda.synchronize()
+            _lib.moe_profile_collect()
+            steps.extend(gi * R + i for i in range(R))
+        del g
+        torch.cuda.synchronize()
+    totals = _lib.moe_profile_totals()
+    _lib.moe_profile_enable(0)
+    return totals, steps
+
+
 # ----------------------------------------------------------------------------- ours
 def run_ours(args, dist):
     import torch
@@ -402,27 +429,13 @@ def run_ours(args, dist):
     gbs = bytes_all / (ms_max * 1e-3) / 1e9
     ms_per_step = ms_max / K
 
-    # per-kernel timing: the same graphs re-captured with event pairs around
-    # every kernel; replayed once each and collected
-    _lib.moe_profile_enable(R * launches_per_step * len(graphs) + 64)
-    pgraphs = []
-    for gi in range(len(graphs)):
-        pgraphs.append(capture(torch, lambda i, b=gi * R: wl.step(b + i, stream), R, stream))
-    torch.cuda.synchronize()
-    for g in pgraphs:  # warm-up replays, not collected
-        with torch.cuda.stream(stream):
-            g.replay()
-    torch.cuda.synchronize()
-    n_prof = 0
-    for rep in range(max(1, min(reps, 16))):
-        with torch.cuda.stream(stream):
-            pgraphs[rep % len(pgraphs)].replay()
-        torch.cuda.synchronize()
-        _lib.moe_profile_collect()
-        n_prof += 1
-    totals = _lib.moe_profile_totals()
-    _lib.moe_profile_enable(0)
-    prof_steps = [((r % len(pgraphs)) * R + i) for r in range(n_prof) for i in range(R)]
+    # per-kernel timing (shares; a tracing aid): the timed sequence of graph
+    # replays once more, each graph re-captured with an event pair around every
+    # kernel; the pairs of one graph are collected after each of its replays
+    # and dropped before the next graph is captured, so exactly K steps (K x
+    # launches per step kernels) are counted, with the bytes of those steps
+    totals, prof_steps = profile_steps(torch, _lib, wl, stream, R, reps, len(graphs),
+                                       launches_per_step)
     kb = {"gateup": 0, "down": 0, "fused_decode": 0}
     for i in prof_steps:
         for kk, v in wl.kernel_bytes(i).items():
@@ -432,18 +445,30 @@ def run_ours(args, dist):
     kern = {}
     for name, (tms, cnt) in totals.items():
         if cnt:
-            kern[name] = {"avg_us": round(tms / cnt * 1e3, 3), "launches": cnt}
+            kern[name] = {"avg_us_event_bracketed": round(tms / cnt * 1e3, 3), "launches": cnt}
     tot_ms = sum(v[0] for v in totals.values())
     for name in kern:
         kern[name]["share"] = round(totals[name][0] / tot_ms, 4) if tot_ms else None
     dom = max(("gateup", "down", "fused_decode"), key=lambda n: totals.get(n, (0, 0))[0])
     dom_ms, dom_cnt = totals[dom]
-    achieved = (kb[dom] / dom_cnt) / (dom_ms / dom_cnt * 1e-3) / 1e9
     traffic = ncu_traffic(dom, "decode_window")
+    if dom == "fused_decode" and launches_per_step == 1:
+        # one kernel per step: its average launch duration in the timed region
+        # is the timed region's time per step (graph replay, CUDA events on the
+        # launching stream; the next launch's set-up overlaps this one's tail)
+        kern_us = ms_max / K * 1e3
+        achieved = bytes_local / K / (kern_us * 1e-6) / 1e9
+        src = "timed region (one launch per step)"
+    else:
+        kern_us = dom_ms / dom_cnt * 1e3
+        achieved = (kb[dom] / dom_cnt) / (kern_us * 1e-6) / 1e9
+        src = "event pairs around each launch"
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                 "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                 "peak_source": peak_src, "traffic": traffic,
-                "algorithmic_bytes_per_launch": kb[dom] // dom_cnt}
+                "algorithmic_bytes_per_launch": (bytes_local // K if src.startswith("timed")
+                                                 else kb[dom] // dom_cnt),
+                "avg_launch_us": round(kern_us, 3), "duration_source": src}
 
     # end to end through the C ABI with host buffers: H2D of the window's
     # logits + activations from pinned memory, the layer, D2H of y/ids/w/n_miss
@@ -456,14 +481,8 @@ def run_ours(args, dist):
         "rows_per_s": round(cfg.T * dist.world / (ms_per_step * 1e-3), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded, random-init int4 experts)",
-        "config": {"workload": "decode_window: 1 layer, T=8 rows, H=2048, E=128 top-8, I=768, "
-                               "shared I=768, Zipf(1.1) logits, int4/32 + fp16 scale",
-                   "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I,
-                   "shared_I": cfg.shared_I,
-                   "l2": f"inputs larger than L2: {N_POOLS} rotating pool copies "
-                         f"({N_POOLS * wl.base.pool_bytes() / 1e9:.2f} GB)",
-                   "parallelism": f"replicas x{dist.world}",
-                   "mean_distinct_experts": round(statistics.mean(wl.distinct), 2)},
+        "config": headline_config(cfg, dist.world),
+        "mean_distinct_experts": round(statistics.mean(wl.distinct), 2),
         "roofline": roofline,
         "kernels": kern,
         "e2e": e2e,
@@ -474,10 +493,38 @@ def run_ours(args, dist):
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     if not args.no_extra and dist.world == 1:
         try:
-            line["configs"] = extra_configs(torch, synth, _lib, dev, stream, hbm_peak, tf_peak)
+            line["configs"] = extra_configs(torch, synth, _lib, dev, stream, hbm_peak, tf_peak,
+                                           cpu_seconds=min(3.0, args.cpu_seconds))
         except Exception as ex:  # the headline line must still print
             line["configs"] = {"error": f"{type(ex).__name__}: {ex}"}
     return line
+
+
+def headline_config(cfg, world: int) -> dict:
+    """The workload of the headline line (both arms print the same dict)."""
+    return {"workload": "decode_window: 1 layer, T=8 rows, H=2048, E=128 top-8, I=768, "
+                        "shared I=768, Zipf(1.1) logits, int4/32 + fp16 scale",
+            "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "shared_I": cfg.shared_I,
+            "l2": f"inputs larger than L2: {N_POOLS} rotating pool copies "
+                  f"({N_POOLS * cfg.E * cfg.expert_bytes() / 1e9:.2f} GB)",
+            "parallelism": f"replicas x{world}"}
+
+
+def host_facts() -> dict:
+    """Core count and CPU model of this host (for the CPU oracle's timings)."""
+    fields = {}
+    try:
+        for line in open("/proc/cpuinfo"):
+            if ":" in line:
+                key, val = (p.strip() for p in line.split(":", 1))
+                fields.setdefault(key.lower(), val)
+    except OSError:
+        pass
+    import platform
+    model = fields.get("model name") or " ".join(
+        f"{k} {fields[k]}" for k in ("cpu implementer", "cpu part") if k in fields)
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.machine(),
+            "machine": platform.machine()}
 
 
 def align_up(n: int, a: int) -> int:
@@ -650,23 +697,51 @@ def cpu_baseline(wl, seconds):
     return {"value": round(byts / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{rows_done} rows of decode windows (1 row each, {el:.1f} s), "
                       f"window bytes scaled by rows/T",
-            "us_per_layer": round(el / rows_done * cfg.T * 1e6, 1)}
+            "us_per_layer": round(el / rows_done * cfg.T * 1e6, 1), **host_facts()}
+
+
+def oracle_rows_timing(inp_host, rows, seconds):
+    """The CPU oracle (one core) on rows of one layer, for at most about
+    `seconds`: -> (seconds per row, rows done)."""
+    import numpy as np
+    import oracle
+    cfg = inp_host.cfg
+    L = oracle.Layer(inp_host)
+    ids, ww, _ = oracle.route(inp_host.logits.numpy(), cfg.k)
+    t0 = time.perf_counter()
+    n = 0
+    while n < len(rows) and (n == 0 or time.perf_counter() - t0 < seconds):
+        L.rows(ids, ww, rows=[rows[n]])
+        n += 1
+    return (time.perf_counter() - t0) / n, n
 
 
 # ----------------------------------------------------------------------------- extras
-def extra_configs(torch, synth, _lib, dev, stream, hbm_peak, tf_peak):
+def extra_configs(torch, synth, _lib, dev, stream, hbm_peak, tf_peak, cpu_seconds=3.0):
+    """The other workloads of the layer, each timed from CUDA graph replays
+    (the whole layer per replay), with weight-pool copies rotated so that a
+    replay's weights are not in L2 from the one before; beside each, the CPU
+    oracle (one core) on a few rows of the same layer, scaled to the layer."""
     from routed_expert_ffn_router_gb300.layer import MoeLayer
-    out = {}
+    out = {"cpu_oracle_host": host_facts()}
 
     def timed(fn, reps):
         with torch.cuda.stream(stream):
             fn(0)
         torch.cuda.synchronize()
-        g = capture(torch, fn, 1, stream)
-        time_graph(torch, [g], 2, stream)
-        return time_graph(torch, [g], reps, stream) / reps
+        g = capture(torch, fn, reps, stream)
+        time_graph(torch, [g], 1, stream)
+        return time_graph(torch, [g], 2, stream) / (2 * reps)
 
-    # expert cache: 16 rows, H 4096, 256 experts top-8, I 1536, 154 resident
+    def cpu_leg(inp, rows, T_layer):
+        if cpu_seconds <= 0:
+            return None
+        s_row, n = oracle_rows_timing(inp.to("cpu"), rows, cpu_seconds)
+        return {"us_per_layer": round(s_row * T_layer * 1e6, 1), "rows_timed": n, "cores": 1,
+                "kind": "oracle", "sample": f"{n} rows of the layer, scaled to {T_layer} rows"}
+
+    # expert cache: 16 rows, H 4096, 256 experts top-8, I 1536, 154 resident;
+    # 4 pool copies (1.63 GB each) in turn
     cfg = synth.EXPERT_CACHE
     inp = synth.make_layer(cfg, 0, device=dev)
     lays = [MoeLayer(inp, cfg.T)] + [MoeLayer(synth.clone_pool(inp), cfg.T) for _ in range(3)]
@@ -679,11 +754,13 @@ def extra_configs(torch, synth, _lib, dev, stream, hbm_peak, tf_peak):
     byts = D * cfg.expert_bytes()
     out["expert_cache"] = {"us_per_layer": round(ms * 1e3, 2), "GB/s": round(byts / ms / 1e6, 1),
                            "frac_hbm": round(byts / ms / 1e6 / hbm_peak, 3),
-                           "distinct_resident": D, "n_miss": int(o["n_miss"].item())}
+                           "distinct_resident": D, "n_miss": int(o["n_miss"].item()),
+                           "l2": "4 rotating pool copies (6.5 GB)",
+                           "cpu_oracle": cpu_leg(inp, list(range(cfg.T)), cfg.T)}
     del lays, inp, o
     torch.cuda.empty_cache()
 
-    # 48 stacked layers, windows of 1..16 rows
+    # 48 stacked layers (43.5 GB of experts), windows of 1..16 rows
     cfg = synth.DECODE_48
     layers = [synth.make_layer(cfg, 0, device=dev, layer=l, T=16) for l in range(cfg.layers)]
     res = {}
@@ -698,29 +775,34 @@ def extra_configs(torch, synth, _lib, dev, stream, hbm_peak, tf_peak):
         def all48(i):
             for m, l, oo in zip(mls, layers, outs):
                 m.forward(l.logits[:T], l.x[:T], out=oo, stream=stream)
-        ms = timed(all48, 8)
+        ms = timed(all48, 4)
         byts = D * cfg.expert_bytes()
         res[f"T{T}"] = {"us_per_layer": round(ms * 1e3 / cfg.layers, 2),
                         "GB/s": round(byts / ms / 1e6, 1),
                         "frac_hbm": round(byts / ms / 1e6 / hbm_peak, 3),
-                        "rows_per_s": round(T / (ms * 1e-3 / cfg.layers), 1)}
+                        "rows_per_s": round(T / (ms * 1e-3 / cfg.layers), 1),
+                        "mean_distinct_experts": round(D / cfg.layers, 2)}
+    res["l2"] = "48 layers in turn (43.5 GB)"
+    res["cpu_oracle_T16"] = cpu_leg(layers[0], list(range(16)), 16)
     out["decode48"] = res
     del layers, mls, outs
     torch.cuda.empty_cache()
 
-    # prefill chunk of 2,048 tokens
+    # prefill chunk of 2,048 tokens; 4 pool copies (0.9 GB each) in turn
     cfg = synth.PREFILL
     inp = synth.make_layer(cfg, 0, device=dev)
-    m = MoeLayer(inp, cfg.T)
-    o = m.forward(inp.logits, inp.x)
+    ms_ = [MoeLayer(inp, cfg.T)] + [MoeLayer(synth.clone_pool(inp), cfg.T) for _ in range(3)]
+    o = ms_[0].forward(inp.logits, inp.x)
     torch.cuda.synchronize()
     D = int(torch.unique(o["ids"]).numel())
-    ms = timed(lambda i: m.forward(inp.logits, inp.x, out=o, stream=stream), 8)
+    ms = timed(lambda i: ms_[i % 4].forward(inp.logits, inp.x, out=o, stream=stream), 8)
     flops = 2 * 3 * cfg.H * cfg.I * (cfg.T * cfg.k) + 2 * 3 * cfg.H * cfg.shared_I * cfg.T
+    rng_rows = [int(r) for r in torch.randperm(cfg.T, generator=torch.Generator().manual_seed(0))[:64]]
     out["prefill"] = {"us_per_layer": round(ms * 1e3, 1), "tok_per_s": round(cfg.T / (ms * 1e-3), 1),
                       "TFLOP/s": round(flops / ms / 1e9, 1),
                       "frac_bf16_peak": round(flops / ms / 1e9 / tf_peak, 4),
-                      "distinct_experts": D}
+                      "distinct_experts": D, "l2": "4 rotating pool copies (3.6 GB)",
+                      "cpu_oracle": cpu_leg(inp, rng_rows, cfg.T)}
     return out
 
 
@@ -775,10 +857,11 @@ def run_profile_case(case: str):
 
 # ----------------------------------------------------------------------------- reference
 def run_reference(args, dist):
-    """The CPU oracle as the reference arm: one sampled row of a decode window
-    per step, scaled to the window; rank 0 only."""
+    """The CPU oracle as the reference arm (rank 0 only), on the headline
+    workload's windows: each step is one sampled row of a window (the oracle
+    takes about 0.2 s per row), its share of the window's algorithmic bytes
+    counted; ms_per_step is the measured time of one such step."""
     import numpy as np
-    import torch
     import oracle
     from routed_expert_ffn_router_gb300 import synth
     if dist.rank != 0:
@@ -808,16 +891,16 @@ def run_reference(args, dist):
     el = time.perf_counter() - t0
     byts = sum(win[i % 16][2] / cfg.T for i in range(K))
     v = byts / el / 1e9
-    ms_step = el / K * 1e3 * cfg.T  # per window
+    sample = (f"one row of a decode window per step ({K} rows, {el:.1f} s), its 1/T share of "
+              f"the window's bytes counted")
     return {"impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "GB/s",
-            "n_gpus": dist.world, "steps": K, "warmup": W, "ms_per_step": round(ms_step, 3),
+            "n_gpus": dist.world, "steps": K, "warmup": W, "ms_per_step": round(el / K * 1e3, 3),
+            "us_per_layer_scaled": round(el / K * cfg.T * 1e6, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, random-init int4 experts)",
-            "config": {"workload": "decode_window: 1 layer, T=8 rows, H=2048, E=128 top-8, I=768, "
-                                   "shared I=768, Zipf(1.1) logits, int4/32 + fp16 scale",
-                       "sample": "one row of a window per step, bytes scaled by 1/T"},
+            "config": headline_config(cfg, dist.world), "sample": sample,
             "cpu_baseline": {"value": round(v, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{K} steps x 1 row"},
+                             "sample": sample, **host_facts()},
             "e2e": {"value": round(v, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

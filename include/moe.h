@@ -102,12 +102,22 @@ typedef struct {
 } moe_qmat;
 
 /* One layer. gate and up have rows = I, K = H; down has rows = H, K = I.
- * The shared expert (shared_I > 0) has one slot of each, with I -> shared_I. */
+ * The shared expert (shared_I > 0) has one slot of each, with I -> shared_I.
+ * pick_counts: routing counters for an adaptive expert cache, counted inside
+ * the engine ("extended-strata-moe reference", "The adaptive cache": picks per
+ * (layer, expert), one per expert and window, large batches not counted).
+ * Nullable device int32 [E], 4-byte aligned; when set, a moe_expert_ffn or
+ * moe_layer_forward call of 1 <= T <= pick_max_rows rows adds 1 to
+ * pick_counts[e] for every distinct expert e its window routes to, resident or
+ * not (atomically, in the call's kernels). moe_cache_observe_device reads and
+ * clears them. Zero-initialise the struct to leave counting off. */
 typedef struct {
   int32_t H, I, E, k, S;
   moe_qmat gate, up, down;
   int32_t shared_I;
   moe_qmat shared_gate, shared_up, shared_down;
+  int32_t *pick_counts;
+  int32_t pick_max_rows;
 } moe_layer_desc;
 
 /* Router logits of the tiny configuration: logits[t][e] = sum_h x[t][h]*wg[h][e]
@@ -175,13 +185,23 @@ moe_status moe_layer_forward(const moe_layer_desc *L, const float *logits, const
  *    16 MiB (e.g. 2,048-token chunks): use moe_expert_ffn with a workspace.
  *  - Every call on a device shares the array and it keeps the last call's
  *    contents; the status word is cleared at each call. Calls that overlap on
- *    the GPU race on it: serialise them. moe_read_status() cannot reach this
- *    array; device-detected problems are not reported through it.
+ *    the GPU race on it: serialise them. Device-detected problems (an expired
+ *    bounded wait, a slot beyond the pool, an id out of range, an h beyond the
+ *    fp16 range) are OR-ed into the array's status word; read it with
+ *    moe_static_read_status() after the call, before the next one.
  *  - The first call on a device looks up the array's address with that device
  *    current; make the first call before any stream capture. */
 moe_status moe_expert_ffn_static(const moe_layer_desc *L, const void *x, moe_dtype x_dtype, int T,
                                  const int32_t *ids, const float *w, const int32_t *slot_map,
                                  float *y, int32_t *miss_ids, int32_t *n_miss, void *stream);
+
+/* Status word of the last moe_expert_ffn_static call on the current device:
+ * copies it on `stream` (after the call's kernels), waits for the stream and
+ * stores the raw bits in *out. Returns MOE_OK (no bit set), MOE_ERR_TIMEOUT
+ * (a bounded wait expired), MOE_ERR_DEVICE (other bits: 1 non-finite logit,
+ * 2 bad slot or id, 8 h out of range), MOE_ERR_INVALID (null out) or
+ * MOE_ERR_CUDA. Like moe_read_status, it synchronises: not for the hot path. */
+moe_status moe_static_read_status(void *stream, int32_t *out);
 
 /* Workspace bytes a call with this layer and T rows needs (256-byte aligned
  * base required); it also serves every call with fewer rows. L is a HOST
@@ -279,6 +299,18 @@ moe_status moe_cache_observe(void *state, int32_t layer, const int32_t *ids, int
 /* The same for every layer of a window at once: ids (HOST int32 [n_layers][T][k]).
  * Every id is validated before any layer is counted. */
 moe_status moe_cache_observe_layers(void *state, const int32_t *ids, int32_t T, int32_t k);
+/* Add picks counted elsewhere: counts (HOST int32 [n_layers][E], >= 0) are
+ * added to the heats, counts[l][e] picks of expert e in layer l (the same as
+ * that many moe_cache_observe windows picking it, with no advance between).
+ * Every count is validated before any is added. */
+moe_status moe_cache_observe_counts(void *state, const int32_t *counts);
+/* The device-side counters of moe_layer_desc.pick_counts for every layer
+ * (DEVICE int32 [n_layers][E], one layer's [E] per desc): copies them to the
+ * host on `stream` (waits for it: call between windows, not in a captured
+ * graph), clears them on `stream` and adds them as moe_cache_observe_counts
+ * does. So the planner needs no per-window copy of the routing ids: the
+ * counters accumulate on the GPU until the planner's next step. */
+moe_status moe_cache_observe_device(void *state, int32_t *counts, void *stream);
 /* Advance the clock by n_tokens generated tokens after a window: heats fade by
  * 2^(-n_tokens / half_life), then the fill round and the swap round run if
  * their clock has come (once each, fills first). swaps (HOST) receives the

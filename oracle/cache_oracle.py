@@ -79,6 +79,15 @@ class CacheOracle:
         for e in picked:
             self.heat[l][e] = self.heat[l][e] + 1.0
 
+    def observe_counts(self, counts):
+        """counts[l][e]: picks counted outside the planner (one per expert and
+        window), added to the heats as they stand."""
+        for l in range(len(self.heat)):
+            for e in range(self.E):
+                c = int(counts[l][e])
+                assert c >= 0
+                self.heat[l][e] = self.heat[l][e] + float(c)
+
     def _cold_hot_lists(self, l):
         """(not held with heat > 0, hottest first), (held, coldest first); ties: lower id."""
         held = set(self.held(l))

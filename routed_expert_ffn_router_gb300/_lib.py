@@ -23,8 +23,9 @@ EXPORTS = ("moe_router_logits", "moe_route", "moe_permute", "moe_expert_ffn", "m
            "moe_workspace_bytes", "moe_workspace_init", "moe_read_status", "moe_status_str",
            "moe_last_launch_count", "moe_profile_enable", "moe_profile_collect",
            "moe_profile_forget", "moe_profile_totals", "moe_profile_kind_name",
-           "moe_expert_ffn_static", "moe_cache_state_bytes", "moe_cache_init",
+           "moe_expert_ffn_static", "moe_static_read_status", "moe_cache_state_bytes", "moe_cache_init",
            "moe_cache_set_resident", "moe_cache_observe", "moe_cache_observe_layers",
+           "moe_cache_observe_counts", "moe_cache_observe_device",
            "moe_cache_advance",
            "moe_cache_rebalance", "moe_cache_slot_map", "moe_cache_heat",
            "moe_cache_swapped_total", "moe_cache_profile_write", "moe_cache_profile_load",
@@ -46,7 +47,8 @@ class moe_layer_desc(ctypes.Structure):
                 ("k", ctypes.c_int32), ("S", ctypes.c_int32),
                 ("gate", moe_qmat), ("up", moe_qmat), ("down", moe_qmat),
                 ("shared_I", ctypes.c_int32),
-                ("shared_gate", moe_qmat), ("shared_up", moe_qmat), ("shared_down", moe_qmat)]
+                ("shared_gate", moe_qmat), ("shared_up", moe_qmat), ("shared_down", moe_qmat),
+                ("pick_counts", ctypes.c_void_p), ("pick_max_rows", ctypes.c_int32)]
 
 
 class moe_cache_params(ctypes.Structure):
@@ -97,11 +99,14 @@ def load(path: str = LIB_PATH):
                                     ctypes.POINTER(ctypes.c_int64)], i32),
             "moe_profile_kind_name": ([ctypes.c_int32], ctypes.c_char_p),
             "moe_expert_ffn_static": ([D, P, i32, i32, P, P, P, P, P, P, P], i32),
+            "moe_static_read_status": ([P, ctypes.POINTER(ctypes.c_int32)], i32),
             "moe_cache_state_bytes": ([ctypes.POINTER(moe_cache_params), P], sz),
             "moe_cache_init": ([P, sz, ctypes.POINTER(moe_cache_params), P], i32),
             "moe_cache_set_resident": ([P, ctypes.c_int32, P, ctypes.c_int32], i32),
             "moe_cache_observe": ([P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32], i32),
             "moe_cache_observe_layers": ([P, P, ctypes.c_int32, ctypes.c_int32], i32),
+            "moe_cache_observe_counts": ([P, P], i32),
+            "moe_cache_observe_device": ([P, P, P], i32),
             "moe_cache_advance": ([P, ctypes.c_int32, P, ctypes.c_int32], ctypes.c_int32),
             "moe_cache_rebalance": ([P, ctypes.c_int32, P, ctypes.c_int32], ctypes.c_int32),
             "moe_cache_slot_map": ([P, ctypes.c_int32, P], i32),
@@ -176,6 +181,16 @@ def moe_expert_ffn_static(desc, x, x_dtype, T, ids, w, slot_map, y, miss_ids, n_
     _check("moe_expert_ffn_static", load().moe_expert_ffn_static(
         ctypes.byref(desc), _ptr(x), x_dtype, T, _ptr(ids), _ptr(w), _ptr(slot_map), _ptr(y),
         _ptr(miss_ids), _ptr(n_miss), _stream(stream)))
+
+
+def moe_static_read_status(stream=None):
+    """-> (moe_status code, raw device status bits) of the last
+    moe_expert_ffn_static call on the current device. Synchronises the stream."""
+    out = ctypes.c_int32(0)
+    code = load().moe_static_read_status(_stream(stream), ctypes.byref(out))
+    if code == MOE_ERR_CUDA:
+        raise MoeError("moe_static_read_status", code, status_str(code))
+    return code, int(out.value)
 
 
 def moe_layer_forward(desc, logits, x, x_dtype, T, slot_map, y, ids, w, miss_ids, n_miss, ws,

@@ -67,6 +67,21 @@ class ExpertCache:
         _lib._check("moe_cache_observe_layers",
                     self.L.moe_cache_observe_layers(self._st(), a.ctypes.data, T, k))
 
+    def observe_counts(self, counts):
+        """Picks counted elsewhere, host int32 [n_layers][E]."""
+        a = np.ascontiguousarray(np.asarray(counts, np.int32))
+        if a.shape != (self.p.n_layers, self.p.n_experts):
+            raise ValueError("counts must be [n_layers][n_experts]")
+        _lib._check("moe_cache_observe_counts", self.L.moe_cache_observe_counts(self._st(), a.ctypes.data))
+
+    def observe_device(self, counts, stream=None):
+        """The device pick counters (a device int32 tensor [n_layers][E], one
+        layer's row per moe_layer_desc.pick_counts): read, cleared and added."""
+        if tuple(counts.shape) != (self.p.n_layers, self.p.n_experts) or not counts.is_contiguous():
+            raise ValueError("counts must be a contiguous [n_layers][n_experts] tensor")
+        _lib._check("moe_cache_observe_device", self.L.moe_cache_observe_device(
+            self._st(), ctypes.c_void_p(counts.data_ptr()), _lib._stream(stream)))
+
     def _out(self, n):
         if n < 0:
             raise _lib.MoeError("moe_cache", _lib.MOE_ERR_INVALID, "invalid argument")

@@ -160,7 +160,14 @@ static moe_status check_desc(const moe_layer_desc* L) {
     if ((s = check_qmat(L->shared_up)) != MOE_OK) return s;
     if ((s = check_qmat(L->shared_down)) != MOE_OK) return s;
   }
+  if (L->pick_counts && ((reinterpret_cast<uintptr_t>(L->pick_counts) & 3u) || L->pick_max_rows < 0))
+    return MOE_ERR_INVALID;
   return MOE_OK;
+}
+
+// The adaptive-cache counters of a call of T rows (nullptr: not counted).
+static int32_t* picks_of(const moe_layer_desc* L, int T) {
+  return L->pick_counts && T >= 1 && T <= L->pick_max_rows ? L->pick_counts : nullptr;
 }
 
 static moe_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
@@ -365,6 +372,7 @@ static moe_status fused_impl(const moe_layer_desc* Ld, const float* logits, cons
   f.partial = at<float>(ws, L.partial);
   f.status = at<int32_t>(ws, L.status);
   f.sync = at<int32_t>(ws, L.sync);
+  f.picks = picks_of(Ld, T);
   return cuda_status(launch_fused_decode(f, st));
 }
 
@@ -396,6 +404,8 @@ static moe_status expert_ffn_impl(const moe_layer_desc* Ld, const void* x, moe_d
   o.status = at<int32_t>(ws, L.status);
   cudaError_t e = launch_permute(ids, T, Ld->E, Ld->k, slot_map, Ld->S, has_shared, o, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (int32_t* picks = picks_of(Ld, T))
+    if ((e = launch_count_picks(o.offsets, Ld->E, picks, st)) != cudaSuccess) return MOE_ERR_CUDA;
 
   FfnArgs a{};
   a.gq = Ld->gate.q; a.gs = Ld->gate.scale;

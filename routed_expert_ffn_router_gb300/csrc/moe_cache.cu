@@ -348,6 +348,32 @@ moe_status moe_cache_observe_layers(void* state, const int32_t* ids, int32_t T, 
   return MOE_OK;
 }
 
+moe_status moe_cache_observe_counts(void* state, const int32_t* counts) {
+  View v;
+  if (!view_of(state, &v) || !counts) return MOE_ERR_INVALID;
+  const size_t LE = (size_t)v.h->p.n_layers * v.h->p.n_experts;
+  for (size_t i = 0; i < LE; ++i)  // validate every count before adding any
+    if (counts[i] < 0) return MOE_ERR_INVALID;
+  for (size_t i = 0; i < LE; ++i) v.heat[i] += (double)counts[i];
+  return MOE_OK;
+}
+
+moe_status moe_cache_observe_device(void* state, int32_t* counts, void* stream) {
+  View v;
+  if (!view_of(state, &v) || !counts) return MOE_ERR_INVALID;
+  const size_t LE = (size_t)v.h->p.n_layers * v.h->p.n_experts;
+  std::vector<int32_t> host(LE);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(host.data(), counts, LE * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(counts, 0, LE * sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return moe_cache_observe_counts(state, host.data());
+}
+
 int32_t moe_cache_advance(void* state, int32_t n_tokens, moe_cache_swap* swaps, int32_t n_max) {
   View v;
   if (!view_of(state, &v) || n_tokens < 0) return -1;

@@ -24,8 +24,11 @@
 //    the 136 + q and 1032 + q code fragments) gets its per-block correction
 //    -magic * sum(B) from one more MMA whose A operand is the constant -magic;
 //  * every CTA computes the top-k ids and the permutation of the whole window
-//    in shared memory, so no launch precedes the weight stream; CTA t computes
-//    row t's float64 softmax weights;
+//    in shared memory, so no launch precedes the weight stream; a helper warp
+//    computes the float64 softmax weights of the rows its CTA reduces (and
+//    writes the routing of the rows whose first output block it owns), so no
+//    CTA waits for another particular CTA: the reduction waits only for the
+//    units, which the CTAs that are running take from the queue;
 //  * once every unit is published, the CTAs share the reduction
 //    y = sum_j w_j sum_g p(e_j, g) + sum_g p(shared, g) in a fixed order, so y is
 //    deterministic; the last CTA to exit resets the cross-CTA counters.
@@ -45,7 +48,7 @@ namespace moe {
 namespace fused {
 
 constexpr int kCW = 8;                  // consumer warps: 4 row warps x 2 column halves
-constexpr int kHelperWarp = kCW + 1;    // routing weights of one row, off the weight stream's path
+constexpr int kHelperWarp = kCW + 1;    // routing weights, off the weight stream's path
 constexpr int kWarps = kCW + 2;         // producer, consumers, helper
 constexpr int kThreads = 32 * kWarps;
 constexpr int kKC = 256;                // columns of K per job
@@ -57,6 +60,8 @@ constexpr int kDnM = kDnRows / (kCW * 16);  // m16 tiles per warp in a down job
 constexpr int kPubCount = kCW * 32;     // arrivals that publish a unit (every consumer lane)
 constexpr int kPubBars = 4;             // publish barriers, used by units in turn
 constexpr int kStgRow = 68;             // floats per token row of a warp's partial staging (64 + 4 pad)
+constexpr int kRedBlock = kCW * 4;      // float4 outputs per CTA and step of the reduction
+constexpr int kBarReduce = 6;           // named barrier: consumers + helper before the reduction
 // Unrolling of the per-block loops of a job (the kernel holds the compute of
 // three unit sizes; full unrolling of all of them crowds the instruction cache:
 // measured on GB300, 2 takes 36.7 us per decode window where 4 takes 38.7 and 1 38.4).
@@ -104,6 +109,7 @@ struct Args {
   float* partial;
   int32_t* status;
   int32_t* sync;
+  int32_t* picks;  // nullable: one pick per distinct expert of the window
 };
 
 // Stage layouts (byte offsets from the 1024-aligned stage base), UI = 32 MT
@@ -447,7 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   __shared__ int s_ids[kMaxT][kMaxK];
   __shared__ uint32_t s_tokmask[kMaxE];
   __shared__ int16_t s_d_of_e[kMaxE];
-  __shared__ float s_topv[kMaxT][kMaxK];  // the selected logits of each row, in rank order
+  // the selected logits of each row in rank order; the helper replaces those of
+  // the rows this CTA reduces by their softmax weights
+  __shared__ float s_rw[kMaxT][kMaxK];
   __shared__ int16_t s_act_e[kMaxE + 1];
   __shared__ int32_t s_act_slot[kMaxE + 1];
   __shared__ int16_t s_act_off[kMaxE + 1];
@@ -457,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   __shared__ uint32_t s_total;
   __shared__ uint32_t s_wsum[kWarps];  // warp sums of the permutation's prefix sum
   __shared__ int s_abort;
+  __shared__ int s_reduce;  // set by consumer thread 0: the units are all published
 
   constexpr int MT = kMT, UI = kUI;  // full units; half units have MT = 2
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -522,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
       else if (E <= 512) bad = topk_row<16>(l, E, k, scr, &s_ids[t][0]);
       else bad = topk_row<32>(l, E, k, scr, &s_ids[t][0]);
       if (bad && lane == 0 && bid == 0) atomicOr(a.status, DEV_NONFINITE_LOGIT);
-      if (lane < k) s_topv[t][lane] = key_value((uint32_t)(scr[kTopkRanked + lane] >> 32));
+      if (lane < k) s_rw[t][lane] = key_value((uint32_t)(scr[kTopkRanked + lane] >> 32));
       __syncwarp();
     }
   } else {
@@ -607,6 +616,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     }
   }
   __syncthreads();
+  // adaptive-cache routing counters: one pick per distinct expert of the window
+  if (a.picks && bid == 0)
+    for (int e = tid; e < E; e += kThreads)
+      if (s_tokmask[e]) atomicAdd(a.picks + e, 1);
   const uint32_t tot = s_total;
   Sched sc;
   sc.D = tot & 0x7ff;
@@ -617,9 +630,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   const int D = sc.D;
   const int nch = H / kKC;        // gate/up jobs (256 columns) per unit
   const int nchd = H / kDnRows;   // down jobs (512 rows) per unit
-  // the reduction waits for every consumer warp's share of every unit and
-  // for the routing-weight rows
-  const int target = sc.total * kCW + (layer_mode ? T : 0);
+  // the reduction waits for every consumer warp's share of every unit
+  const int target = sc.total * kCW;
+  // reduction blocks of kRedBlock float4 outputs: block b is row b / nbr of y,
+  // reduced by CTA b mod G (H is a multiple of 512, so a block never spans rows)
+  const int nbr = H / (4 * kRedBlock), nblk = T * nbr;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -663,23 +678,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     }
     __syncwarp();
   } else if (warp == kHelperWarp) {
-    // ================= helper: routing weights of row bid =================
-    // softmax over the k selected logits in rank order, one rounding to fp32;
-    // published like a unit (the reduction waits for T of them)
-    if (layer_mode && bid < T) {
-      const int t = bid;
-      const float v = lane < k ? s_topv[t][lane] : 0.f;
-      const float wv = topk_softmax_weight(v, k);
-      if (lane < k) {
-        a.ids_out[(size_t)t * k + lane] = s_ids[t][lane];
-        a.w_out[(size_t)t * k + lane] = wv;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence();
-        atomicAdd(a.sync + kSyncUnits, 1);
+    // ================= helper: routing weights of the rows this CTA reduces =================
+    // softmax over the k selected logits in rank order, one rounding to fp32,
+    // into s_rw; the routing of a row goes out from the CTA that reduces its
+    // first block. Then the helper arrives at the reduction's barrier.
+    if (layer_mode) {
+      int prev = -1;
+      for (int b = bid; b < nblk; b += G) {
+        const int t = b / nbr;
+        if (t == prev) continue;
+        prev = t;
+        const float v = lane < k ? s_rw[t][lane] : 0.f;
+        const float wv = topk_softmax_weight(v, k);
+        __syncwarp();
+        if (lane < k) {
+          s_rw[t][lane] = wv;
+          if (b == t * nbr) {
+            a.ids_out[(size_t)t * k + lane] = s_ids[t][lane];
+            a.w_out[(size_t)t * k + lane] = wv;
+          }
+        }
       }
     }
+    __syncwarp();
+    named_bar_arrive(kBarReduce, kCW * 32 + 32);
   } else {
     // ================= consumers =================
     const int cw = warp - 1, mw = cw & 3, kh = cw >> 2, ct = tid - 32;
@@ -895,13 +917,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     // (g in order; n the group's down partial, A + B from its halves if it was split),
     // and y = v_0 + ... + v_7 in lane order: a fixed order on every CTA, for any
     // window and any split.
-    if (!*abort_flag) {
-      if (ct == 0 && !wait_counter_bounded(a.sync + kSyncUnits, target, a.status)) *abort_flag = 1;
-      named_bar_sync(6, kCW * 32);
-      if (!*abort_flag) {
+    // One thread decides for all (the abort flag may still change meanwhile),
+    // and every consumer and the helper meet at the barrier unconditionally.
+    if (ct == 0) {
+      bool go = !*abort_flag;
+      if (go && !wait_counter_bounded(a.sync + kSyncUnits, target, a.status)) {
+        *abort_flag = 1;
+        go = false;
+      }
+      s_reduce = go ? 1 : 0;
+    }
+    named_bar_sync(kBarReduce, kCW * 32 + 32);
+    {
+      if (s_reduce) {
         const int q = ct & 7, H4 = H / 4, NO = T * H4;
         const size_t gstride = (size_t)a.Gh * H;
-        for (int o0 = bid * (kCW * 4); o0 < NO; o0 += G * (kCW * 4)) {
+        for (int o0 = bid * kRedBlock; o0 < NO; o0 += G * kRedBlock) {
           const int o = o0 + (ct >> 3);
           const bool live = o < NO;
           const int t = live ? o / H4 : 0, col = live ? (o - t * H4) * 4 : 0;
@@ -915,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
               const int dd = s_d_of_e[e];
               if (dd < 0) continue;
               const int pos = s_act_off[dd] + __popc(s_tokmask[e] & ((1u << t) - 1u));
-              const float wv = layer_mode ? ldg_cg_f32(a.w_out + (size_t)t * k + jj) : a.w_in[(size_t)t * k + jj];
+              const float wv = layer_mode ? s_rw[t][jj] : a.w_in[(size_t)t * k + jj];
               const float* pp = a.partial + (size_t)pos * gstride + col;
               float4 sacc = make_float4(0.f, 0.f, 0.f, 0.f);
               for (int g0 = 0; g0 < sc.nGi; g0 += 8) {  // 8 groups' loads in flight
@@ -977,13 +1008,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
 }  // namespace fused
 
 // Host side -------------------------------------------------------------------
+// SM count of the current device (cached per device: the grid is one CTA per SM).
 static int num_sms() {
-  static int n = 0;
+  constexpr int kMaxDev = 64;
+  static int n_of[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  if (dev < 0 || dev >= kMaxDev) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+  }
+  int n = __atomic_load_n(&n_of[dev], __ATOMIC_RELAXED);
   if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 1;
+    }
+    __atomic_store_n(&n_of[dev], n, __ATOMIC_RELAXED);
   }
   return n;
 }
@@ -1150,18 +1195,25 @@ static cudaError_t launch_nt(fused::Args& a, cudaStream_t st) {
   a.nst = stages_for<NTX>(a.TB);
   if (a.nst < 2) return cudaErrorInvalidValue;
   const size_t smem = fused::smem_bytes(MT, NTX, a.nst, a.stage_bytes, a.TB);
+  // the shared-memory opt-in is a per-device attribute of the function
   static std::mutex mu;
-  static size_t configured = 0;
+  static size_t configured[64] = {};
   {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+      cudaGetLastError();
+      return e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    }
     std::lock_guard<std::mutex> lk(mu);
-    if (smem > configured) {
-      cudaError_t e = cudaFuncSetAttribute(fused::decode_layer_kernel<NTX>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (smem > configured[dev]) {
+      e = cudaFuncSetAttribute(fused::decode_layer_kernel<NTX>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) {
         cudaGetLastError();
         return e;
       }
-      configured = smem;
+      configured[dev] = smem;
     }
   }
   // programmatic dependent launch: the kernel's set-up overlaps the end of the
@@ -1223,6 +1275,7 @@ cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st) {
   a.miss_ids = f.miss_ids; a.n_miss = f.n_miss;
   a.partial = f.partial;
   a.status = f.status; a.sync = f.sync;
+  a.picks = f.picks;
   return TB == 8 ? launch_nt<1>(a, st) : launch_nt<2>(a, st);
 }
 

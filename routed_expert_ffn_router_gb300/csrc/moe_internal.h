@@ -73,6 +73,8 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, const int32_
                            bool has_shared, const PermuteOut& o, cudaStream_t st);
 cudaError_t launch_ffn_decode(const FfnArgs& a, const void* x, bool x_bf16, int cu_max,
                               cudaStream_t st);
+// counts[e] += 1 for every expert with rows in the permutation (offsets [E+1]).
+cudaError_t launch_count_picks(const int32_t* offsets, int E, int32_t* counts, cudaStream_t st);
 
 int cu_bound(int T, int E, int k, bool has_shared);
 cudaError_t launch_combine(const FfnArgs& a, cudaStream_t st);
@@ -106,6 +108,7 @@ struct FusedLaunch {
   float* partial;
   int32_t* status;
   int32_t* sync;
+  int32_t* picks;  // nullable: +1 per distinct routed expert (adaptive-cache counters)
 };
 bool fused_decode_supported(int H, int I, int shI, int T, bool x_bf16);
 // Slices of I per partial row of the one-launch path (the partial buffer holds

@@ -266,4 +266,19 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, const int32_
   return cudaGetLastError();
 }
 
+// Adaptive-cache routing counters ("extended-strata-moe reference", "The
+// adaptive cache": picks per (layer, expert), one per expert and window): an
+// expert with rows in the window's permutation gets one pick.
+__global__ void count_picks_kernel(const int32_t* offsets, int E, int32_t* counts) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e < E && offsets[e + 1] > offsets[e]) atomicAdd(counts + e, 1);
+}
+
+cudaError_t launch_count_picks(const int32_t* offsets, int E, int32_t* counts, cudaStream_t st) {
+  launch_begin(K_PERMUTE, st);
+  count_picks_kernel<<<(E + 255) / 256, 256, 0, st>>>(offsets, E, counts);
+  launch_end(st);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

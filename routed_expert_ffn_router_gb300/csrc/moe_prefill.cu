@@ -644,21 +644,26 @@ bool b_maps(CUtensorMap* m, const void* p, int cols, int rows) {
 template <bool GU>
 cudaError_t pf_launch(pf::Args& a, cudaStream_t st) {
   const size_t smem = pf::smem_bytes<GU>();
+  // the shared-memory opt-in is a per-device attribute of the function
   static std::mutex mu;
-  static bool configured = false;
+  static bool configured[64] = {};
+  int dev = 0, sms = 0;
   {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+      cudaGetLastError();
+      return e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    }
     std::lock_guard<std::mutex> lk(mu);
-    if (!configured) {
-      cudaError_t e = cudaFuncSetAttribute(pf::pf_kernel<GU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (!configured[dev]) {
+      e = cudaFuncSetAttribute(pf::pf_kernel<GU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) {
         cudaGetLastError();
         return e;
       }
-      configured = true;
+      configured[dev] = true;
     }
   }
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   launch_begin(GU ? K_GATEUP : K_DOWN, st);
   pf::pf_kernel<GU><<<sms > 0 ? sms : 1, pf::kThreads, smem, st>>>(a);

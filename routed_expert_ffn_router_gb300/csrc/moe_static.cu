@@ -11,7 +11,8 @@
 // library until the process exits). It calls no allocating routine.
 //
 // The array is shared by every call on a device and keeps the last call's
-// contents; the status word at its start is cleared on each call. Calls that
+// contents; the status word at its start is cleared on each call and read
+// back by moe_static_read_status. Calls that
 // overlap on the GPU (other streams, other host threads) race on the array and
 // must be serialised by the caller. The first call on a device looks up the
 // array's device address (once, with that device current); make that first
@@ -72,4 +73,11 @@ extern "C" moe_status moe_expert_ffn_static(const moe_layer_desc* L, const void*
   }
   return moe_expert_ffn(L, x, x_dtype, T, ids, w, slot_map, y, miss_ids, n_miss, ws,
                         kStaticScratchBytes, stream);
+}
+
+extern "C" moe_status moe_static_read_status(void* stream, int32_t* out) {
+  if (!out) return MOE_ERR_INVALID;
+  void* ws = static_scratch_ptr();
+  if (!ws) return MOE_ERR_CUDA;
+  return moe_read_status(ws, stream, out);
 }

@@ -292,3 +292,40 @@ def test_copy_moves_fills_the_pool_slots():
     for _, slot, e_in, _ in moves:
         for name in POOL_TENSORS:
             assert torch.equal(getattr(pool, name)[slot], getattr(store, name)[e_in])
+
+
+def test_observe_counts_matches_the_oracle_and_per_window_picks():
+    """Picks counted outside the planner (the device counters) enter the heat
+    as the oracle adds them, bit for bit; with no advance between the windows
+    they equal the per-window picks to the last bits of the double sum."""
+    rng = np.random.default_rng(12)
+    L, E, k = 3, 40, 4
+    lib_c = ExpertCache(L, E, [8, 40, 0])
+    orc = CacheOracle(L, E, [8, 40, 0])
+    per_win = ExpertCache(L, E, [8, 40, 0])
+    for step in range(6):
+        counts = np.zeros((L, E), np.int32)
+        for _ in range(5):  # five windows between planner steps
+            ids = rng.integers(0, E, size=(L, 4, k)).astype(np.int32)
+            for l in range(L):
+                counts[l, np.unique(ids[l])] += 1
+                per_win.observe(l, ids[l])
+        lib_c.observe_counts(counts)
+        orc.observe_counts(counts.tolist())
+        for l in range(L):
+            assert lib_c.heat(l).tobytes() == np.asarray(orc.heat[l], np.float64).tobytes()
+            np.testing.assert_allclose(lib_c.heat(l), per_win.heat(l), rtol=1e-12, atol=0)
+        assert lib_c.advance(3) == [tuple(m) for m in orc.advance(3)]
+        per_win.advance(3)
+
+
+def test_observe_counts_rejects_negative_counts():
+    c = ExpertCache(2, 8, [2, 2])
+    bad = np.zeros((2, 8), np.int32)
+    bad[1, 3] = -1
+    bad[0, 0] = 5
+    with pytest.raises(_lib.MoeError):
+        c.observe_counts(bad)
+    assert c.heat(0)[0] == 0.0  # validated before anything was added
+    with pytest.raises(ValueError):
+        c.observe_counts(np.zeros((1, 8), np.int32))

@@ -234,7 +234,33 @@ def test_decode48_layers(T):
         hinp = inp.to("cpu")
         ids, w, we, y = oracle_layer(hinp, hinp.logits.numpy())
         assert np.array_equal(out["ids"], ids)
+        assert_weights_match(out["w"], w, we)
         check_y(out["y"], y, what=f"decode48 T={T} layer {layer}")
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_decode48_near_tied_logits_route_bit_exact(T):
+    """The one-launch decode kernel routes the window itself (every CTA runs the
+    top-k; the softmax weights come from the kernel's own float-float path): at
+    512 experts top-10 with logits on a grid of 1/4, so that many are exactly
+    equal, its ids and fp32 weights must equal the oracle's bit for bit and ties
+    must go to the lower expert id."""
+    cfg = synth.DECODE_48
+    inp = synth.make_layer(cfg, 0, device=DEV, layer=3, T=T)
+    rng = np.random.default_rng(40 + T)
+    lg = (np.round(rng.normal(size=(T, cfg.E)) * 2) / 4).astype(np.float32)
+    lg[0, :] = np.float32(-1.0)
+    lg[0, 100:140] = np.float32(0.5)  # 40 equal maxima: ids 100..109 must be taken
+    if T > 1:
+        lg[1, :] = np.float32(0.0)     # all equal, with signed zeros
+        lg[1, ::3] = np.float32(-0.0)
+    out, _ = run_layer(inp, logits=torch.from_numpy(lg))
+    hinp = inp.to("cpu")
+    ids, w, we, y = oracle_layer(hinp, lg)
+    assert list(ids[0]) == list(range(100, 110))
+    assert np.array_equal(out["ids"], ids)
+    assert_weights_match(out["w"], w, we)
+    check_y(out["y"], y, what=f"decode48 near-tied T={T}")
 
 
 def test_expert_cache_random_slot_map_and_misses():
@@ -279,7 +305,8 @@ def test_prefill_random_slot_map_and_misses():
 
 def test_prefill_sampled_rows():
     """2,048-token chunk: every output row is finite; the oracle checks sampled
-    rows, including rows routed to the hottest expert, the first and the last."""
+    rows, including rows routed to the hottest expert, the rows with the most
+    picks of experts of at most 16 tokens, the first and the last."""
     cfg = synth.PREFILL
     inp = synth.make_layer(cfg, 0, device=DEV)
     out, _ = run_layer(inp)
@@ -288,11 +315,17 @@ def test_prefill_sampled_rows():
     assert np.array_equal(out["ids"], ids)
     assert_weights_match(out["w"], w, we)
     assert np.all(np.isfinite(out["y"]))
-    hot = np.bincount(ids.ravel(), minlength=cfg.E).argmax()
+    counts = np.bincount(ids.ravel(), minlength=cfg.E)
+    hot = counts.argmax()
     rows_hot = np.nonzero((ids == hot).any(1))[0]
+    # the rows with the most picks of light experts (at most 16 tokens: the jobs
+    # that take the smallest token boxes); under this skew a row has 2-3 of them
+    n_light = (counts[ids] <= 16).sum(1)
+    rows_light = np.argsort(-n_light, kind="stable")[:4]
+    assert n_light[rows_light[0]] >= 2
     rng = np.random.default_rng(0)
     rows = sorted(set([0, cfg.T - 1] + list(rng.choice(cfg.T, 10, replace=False)) +
-                      list(rows_hot[:3]) + list(rows_hot[-3:])))
+                      list(rows_hot[:3]) + list(rows_hot[-3:]) + list(rows_light)))
     y = oracle.Layer(hinp).rows(ids, w, rows=rows)
     check_y(out["y"][rows], y, what="prefill sampled rows")
 
@@ -304,6 +337,7 @@ def test_ragged_windows(T):
     out, _ = run_layer(inp)
     ids, w, we, y = oracle_layer(inp, inp.logits.numpy())
     assert np.array_equal(out["ids"], ids)
+    assert_weights_match(out["w"], w, we)
     check_y(out["y"], y, what=f"T={T}")
 
 

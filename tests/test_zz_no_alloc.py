@@ -32,24 +32,55 @@ def _route(lg, k):
     return ids, w
 
 
-def test_static_scratch_matches_workspace_entry_point_twice():
-    cfg = synth.MoeConfig("noalloc", H=2048, I=768, E=128, k=8, T=8, shared_I=768, zipf_s=1.1)
-    inp = synth.make_layer(cfg, 21, device="cuda")
+def _cache_layer(cfg, seed):
+    """A layer whose pool holds only 60% of the experts (slot map with misses)."""
+    inp = synth.make_layer(cfg, seed)
+    smt, S = synth.random_slot_map(cfg.E, 0.6, seed=seed + 1)
+    keep = (smt >= 0).nonzero().flatten()
+    for kname in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s"):
+        setattr(inp, kname, getattr(inp, kname)[keep].contiguous())
+    inp.S = S
+    inp.slot_map = smt
+    return inp.to("cuda")
+
+
+# Three routes through the library, each placing different regions in the
+# scratch: the one-launch decode kernel (bf16 rows), the separate permute /
+# gate-up / down / combine kernels (fp32 rows), and a slot map with misses.
+CASES = {
+    "decode_bf16": (synth.MoeConfig("noalloc", H=2048, I=768, E=128, k=8, T=8, shared_I=768,
+                                    zipf_s=1.1), False),
+    "separate_f32": (synth.MoeConfig("noalloc_f32", H=256, I=128, E=16, k=4, T=6, shared_I=128,
+                                     zipf_s=1.0, x_dtype="f32"), False),
+    "slot_map_misses": (synth.MoeConfig("noalloc_cache", H=1024, I=512, E=64, k=8, T=16,
+                                        zipf_s=1.2), True),
+}
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_static_scratch_matches_workspace_entry_point_twice(case):
+    cfg, cached = CASES[case]
+    inp = _cache_layer(cfg, 21) if cached else synth.make_layer(cfg, 21, device="cuda")
     lay = MoeLayer(inp, T_max=cfg.T)
+    sm = inp.slot_map if cached else None
     logits, xs = synth.draw_windows(inp, 2, seed=5)
     for call in range(2):  # two calls in a row, different windows
         ids, w = _route(logits[call], cfg.k)
-        ref = lay.expert_ffn(xs[call], ids, w)
+        ref = lay.expert_ffn(xs[call], ids, w, slot_map=sm)
         y = torch.full((cfg.T, cfg.H), float("nan"), device="cuda")
         miss = torch.full((cfg.E,), -5, dtype=torch.int32, device="cuda")
         nm = torch.full((1,), -5, dtype=torch.int32, device="cuda")
-        _lib.moe_expert_ffn_static(lay.desc, xs[call], _lib.MOE_BF16, cfg.T, ids, w, None, y, miss,
+        _lib.moe_expert_ffn_static(lay.desc, xs[call], lay.x_dtype, cfg.T, ids, w, sm, y, miss,
                                    nm)
-        torch.cuda.synchronize()
+        code, bits = _lib.moe_static_read_status()
+        assert code == _lib.MOE_OK, (call, bits)
         y_ref = ref["y"].double().cpu().numpy()
         err = np.abs(y.double().cpu().numpy() - y_ref).max()
         assert err <= TOL * np.abs(y_ref).max(), (call, err)
-        assert int(nm.item()) == int(ref["n_miss"].item()) == 0
+        n = int(ref["n_miss"].item())
+        assert int(nm.item()) == n
+        assert (n > 0) == cached
+        assert torch.equal(miss[:n], ref["miss_ids"][:n])
 
 
 def test_static_scratch_rejects_a_chunk_too_large_for_it():
