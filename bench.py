@@ -48,7 +48,8 @@ def parse():
                     help="skip the secondary configurations (prefill, 48-layer decode, expert cache)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="bound on the oracle's CPU time for cpu_baseline")
-    ap.add_argument("--profile-case", choices=["decode_window", "prefill"], default=None,
+    ap.add_argument("--profile-case", choices=["decode_window", "prefill", "expert_cache",
+                                               "decode48_T1"], default=None,
                     help="run a few eager launches of one small case and exit (the target "
                          "of ncu captures: about 1 GB on the device, inputs larger than L2)")
     return ap.parse_args()
@@ -249,9 +250,10 @@ def csrc_hash(kernel: str = "fused_decode") -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel sources
-    have not changed since it was taken (else None)."""
+def ncu_traffic(kernel: str, workload: str, algorithmic_bytes: float):
+    """DRAM bytes per launch from a committed ncu summary (the captured launch's
+    DRAM bytes over its algorithmic bytes, times this run's algorithmic bytes per
+    launch), if the kernel sources have not changed since it was taken (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -259,7 +261,7 @@ def ncu_traffic(kernel: str, workload: str):
         d = json.load(open(p))
         ent = d.get(workload, {}).get(kernel)
         if ent and ent.get("csrc_sha") == csrc_hash(kernel):
-            return ent.get("dram_bytes_per_launch")
+            return int(round(ent["traffic_ratio"] * algorithmic_bytes))
     except Exception:
         return None
     return None
@@ -451,7 +453,6 @@ def run_ours(args, dist):
         kern[name]["share"] = round(totals[name][0] / tot_ms, 4) if tot_ms else None
     dom = max(("gateup", "down", "fused_decode"), key=lambda n: totals.get(n, (0, 0))[0])
     dom_ms, dom_cnt = totals[dom]
-    traffic = ncu_traffic(dom, "decode_window")
     if dom == "fused_decode" and launches_per_step == 1:
         # one kernel per step: its average launch duration in the timed region
         # is the timed region's time per step (graph replay, CUDA events on the
@@ -463,11 +464,12 @@ def run_ours(args, dist):
         kern_us = dom_ms / dom_cnt * 1e3
         achieved = (kb[dom] / dom_cnt) / (kern_us * 1e-6) / 1e9
         src = "event pairs around each launch"
+    alg_per_launch = bytes_local // K if src.startswith("timed") else kb[dom] // dom_cnt
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                 "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                "peak_source": peak_src, "traffic": traffic,
-                "algorithmic_bytes_per_launch": (bytes_local // K if src.startswith("timed")
-                                                 else kb[dom] // dom_cnt),
+                "peak_source": peak_src,
+                "traffic": ncu_traffic(dom, "decode_window", alg_per_launch),
+                "algorithmic_bytes_per_launch": alg_per_launch,
                 "avg_launch_us": round(kern_us, 3), "duration_source": src}
 
     # end to end through the C ABI with host buffers: H2D of the window's
@@ -824,6 +826,18 @@ def run_profile_case(case: str):
         fn = wl.step
         n = 6
         lay = wl.layers[0]
+    elif case in ("expert_cache", "decode48_T1"):
+        # one pool (expert cache: 1.63 GB; one 48-layer-shaped layer: 0.9 GB)
+        # and 4 windows of fresh logits and rows
+        cfg = synth.EXPERT_CACHE if case == "expert_cache" else synth.DECODE_48.with_T(1)
+        inp = synth.make_layer(cfg, 0, device=dev, **({} if case == "expert_cache" else {"T": 1}))
+        lay = MoeLayer(inp, T_max=cfg.T)
+        logits, xs = synth.draw_windows(inp, 4, seed=3, device=dev)
+        out = lay.alloc_outputs(cfg.T)
+
+        def fn(i):
+            lay.forward(logits[i % 4], xs[i % 4], out=out)
+        n = 6
     else:
         cfg = synth.PREFILL
         inp = synth.make_layer(cfg, 0, device=dev)

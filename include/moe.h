@@ -49,10 +49,12 @@
  *    a row's output does not depend on the other rows of the window.
  *  - A workspace serves one call at a time: calls that share one must be
  *    ordered (one stream, or events). The one-launch decode kernel runs one
- *    CTA per SM and its CTAs wait for each other's results, so it expects the
- *    whole GPU: a kernel running beside it on another stream can keep some of
- *    its CTAs from starting, and then its waits expire (MOE_ERR_TIMEOUT from
- *    moe_read_status; re-initialise the workspace and repeat the call).
+ *    CTA per SM; its work units go to whichever CTAs are running and its
+ *    final reduction waits only for those units, so a CTA that starts late
+ *    (SMs held by a kernel on another stream) delays the call without
+ *    stalling the others. If a wait does expire (about a second; e.g. a
+ *    workspace left inconsistent by an interrupted call), moe_read_status
+ *    reports MOE_ERR_TIMEOUT: re-initialise the workspace and repeat the call.
  *
  * Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32), H and I (and shared_I)
  * multiples of 128 and at most 16384, T >= 0 (T = 0 is a no-op that reports
@@ -336,6 +338,56 @@ int64_t moe_cache_swapped_total(const void *state);
  * profile order (a repeated pair is skipped); the rank table is not read. */
 int64_t moe_cache_profile_write(const void *state, uint8_t *buf, int64_t n_max);
 moe_status moe_cache_profile_load(void *state, const uint8_t *buf, int64_t n);
+
+/* ---- Mailbox: the missed experts, computed on the host ----
+ * "extended-strata-moe reference", "The mailbox": the GPU computes the experts
+ * its slot map holds and hands the rows routed to the others to host threads,
+ * which compute those experts from the host copy of every expert and hand back
+ * partial outputs; the GPU adds them to y in a fixed order. A job is one expert
+ * over up to 8 of its rows (the multi-token CPU kernels of Strata BATCHING), so
+ * a job reads the expert's weights once. The flow of one window:
+ *   1. moe_layer_forward / moe_expert_ffn with the slot map (y holds the
+ *      resident experts and the shared expert);
+ *   2. copy ids, w (and x, if not on the host already) back; moe_mailbox_pairs
+ *      lists the pairs p = t*k + j whose expert is not held, ascending;
+ *   3. moe_mailbox_compute fills partial[i] = w_p * down(silu(gate x_t) * (up
+ *      x_t)) for the i-th listed pair p, on the mailbox's threads (fp32);
+ *   4. copy pairs and partials to the device; moe_mailbox_add adds, for every
+ *      row t, its partials in list order (ascending j) to y[t].
+ * The result is deterministic (each partial is one thread's fixed computation;
+ * the sums run in list order).
+ *  moe_mailbox_create(n_threads, timeout_ms): a pool of host threads; a compute
+ *      call waits at most timeout_ms for its jobs. NULL for bad arguments.
+ *  moe_mailbox_destroy: joins the threads.
+ *  moe_mailbox_pairs: ids (HOST [T][k]), slot_map (HOST [E], -1 = not held) ->
+ *      pairs (HOST, ascending) of the pairs whose expert is not held; returns
+ *      their number (pairs NULL: only counts), or -1 (bad argument, an id
+ *      outside [0, E), more than n_max pairs).
+ *  moe_mailbox_compute: L describes a HOST store of every expert (slot = expert
+ *      id: its gate/up/down q and scale pointers are host pointers, S >= E;
+ *      shared expert ignored), x (HOST [T][H], x_dtype), ids and w (HOST
+ *      [T][k]), pairs (HOST, strictly ascending, from moe_mailbox_pairs),
+ *      partial (HOST [n_pairs][H] fp32, written). Returns MOE_OK, MOE_ERR_INVALID
+ *      (bad argument or pair list), or MOE_ERR_TIMEOUT: a job did not come back
+ *      in time (a stalled or lost thread); partial is then incomplete, no
+ *      thread writes it or reads the caller's buffers after the call returns,
+ *      and the mailbox serves the next call.
+ *  moe_mailbox_inject(mb, mode): failure injection for tests, on the host: the
+ *      next job taken stalls past the timeout (1) or is lost (2); 0 clears.
+ *  moe_mailbox_add: partial (DEVICE [n][H] fp32, 16-byte aligned), pairs
+ *      (DEVICE [n], ascending), y (DEVICE [T][H], 16-byte aligned): one kernel
+ *      on `stream`; H a multiple of 4, T <= 65535. */
+typedef struct moe_mailbox moe_mailbox;
+moe_mailbox *moe_mailbox_create(int32_t n_threads, int32_t timeout_ms);
+void moe_mailbox_destroy(moe_mailbox *mb);
+int32_t moe_mailbox_pairs(const int32_t *ids, int32_t T, int32_t k, const int32_t *slot_map, int32_t E,
+                          int32_t *pairs, int32_t n_max);
+moe_status moe_mailbox_compute(moe_mailbox *mb, const moe_layer_desc *L, const void *x, moe_dtype x_dtype,
+                               int32_t T, const int32_t *ids, const float *w, const int32_t *pairs,
+                               int32_t n_pairs, float *partial);
+moe_status moe_mailbox_inject(moe_mailbox *mb, int32_t mode);
+moe_status moe_mailbox_add(const float *partial, const int32_t *pairs, int32_t n, int32_t T, int32_t k,
+                           int32_t H, float *y, void *stream);
 
 /* ---- Routing traces (host side) ----
  * "extended-strata-moe reference", "Routing trace format": one record per

@@ -29,7 +29,8 @@ EXPORTS = ("moe_router_logits", "moe_route", "moe_permute", "moe_expert_ffn", "m
            "moe_cache_advance",
            "moe_cache_rebalance", "moe_cache_slot_map", "moe_cache_heat",
            "moe_cache_swapped_total", "moe_cache_profile_write", "moe_cache_profile_load",
-           "moe_trace_write", "moe_trace_read")
+           "moe_trace_write", "moe_trace_read", "moe_mailbox_create", "moe_mailbox_destroy",
+           "moe_mailbox_pairs", "moe_mailbox_compute", "moe_mailbox_inject", "moe_mailbox_add")
 
 
 class MoeError(RuntimeError):
@@ -117,6 +118,14 @@ def load(path: str = LIB_PATH):
             "moe_trace_write": ([ctypes.c_int32, P, P, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int64],
                                 ctypes.c_int64),
             "moe_trace_read": ([P, ctypes.c_int64, P, P, P, P, ctypes.c_int32, ctypes.c_int64], ctypes.c_int64),
+            "moe_mailbox_create": ([ctypes.c_int32, ctypes.c_int32], P),
+            "moe_mailbox_destroy": ([P], None),
+            "moe_mailbox_pairs": ([P, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int32, P, ctypes.c_int32],
+                                  ctypes.c_int32),
+            "moe_mailbox_compute": ([P, D, P, i32, ctypes.c_int32, P, P, P, ctypes.c_int32, P], i32),
+            "moe_mailbox_inject": ([P, ctypes.c_int32], i32),
+            "moe_mailbox_add": ([P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P],
+                                i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)

@@ -20,9 +20,11 @@
 //  * gate/up tiles interleave 8 gate rows and the same 8 up rows, so an MMA
 //    accumulator holds g and u of one intermediate index side by side and
 //    SwiGLU happens in registers; h is kept as fp16 in the down operand's
-//    fragment order. The exact-integer warp-MMA core (moe_decode.cu explains
-//    the 136 + q and 1032 + q code fragments) gets its per-block correction
-//    -magic * sum(B) from one more MMA whose A operand is the constant -magic;
+//    fragment order (h / 16 where it meets a high nibble). The exact-integer
+//    warp-MMA core (moe_decode.cu explains the 136 + q and 1032 + q code
+//    fragments; the down MMA takes high nibbles in place as 1152 + 16 q) gets
+//    its per-block correction -magic * sum(B) from one more MMA whose A operand
+//    is the constant -magic;
 //  * every CTA computes the top-k ids and the permutation of the whole window
 //    in shared memory, so no launch precedes the weight stream; a helper warp
 //    computes the float64 softmax weights of the rows its CTA reduces (and
@@ -137,6 +139,22 @@ __host__ __device__ inline size_t smem_bytes(int MT, int NTX, int nst, int stage
 // The slot map's copy lives in stage memory during the routing (after the
 // top-k scratch of every warp), before the first weight copy.
 constexpr int kSlotMapOff = 32768;
+
+// Four f16x2 registers from one word of int4 codes for the down MMA, without
+// shifts per nibble: registers 0 and 2 hold the low nibbles of bytes (0, 2)
+// and (1, 3) as 1032 + code, registers 1 and 3 the high nibbles as
+// 1152 + 16 code (the nibble stays in place under the f16 constant 1024, bit 3
+// of the nibble flipped). The h operand holds h / 16 at the high-nibble
+// positions, so those products are (72 + code) h and the correction constant
+// there is -1152 (times h / 16). Same register pairing as dequant_word_f16.
+__device__ __forceinline__ void dequant_word_f16x16(uint32_t w, uint32_t (&d)[4]) {
+  d[0] = lop3_and_xor(w, 0x000F000Fu, 0x64086408u);
+  d[1] = lop3_and_xor(w, 0x00F000F0u, 0x64806480u);
+  const uint32_t w8 = w >> 8;
+  d[2] = lop3_and_xor(w8, 0x000F000Fu, 0x64086408u);
+  d[3] = lop3_and_xor(w8, 0x00F000F0u, 0x64806480u);
+}
+constexpr uint32_t kF16NegMagicHi = 0xE480E480u;  // f16 -1152
 
 // n-th (0-based) set bit of a mask (mask has more than n bits set).
 __device__ __forceinline__ int nth_bit(uint32_t m, int n) {
@@ -272,8 +290,9 @@ __device__ __forceinline__ void dn_compute(uint32_t st, uint32_t hb, int cw, int
       bf[nt][0] = v.x; bf[nt][1] = v.y; bf[nt][2] = v.z; bf[nt][3] = v.w;
 #pragma unroll
       for (int q = 0; q < 4; ++q) corr[nt][q] = 0.f;
-      mma_f16_16816(corr[nt], kF16NegMagic, kF16NegMagic, kF16NegMagic, kF16NegMagic, bf[nt][0], bf[nt][1]);
-      mma_f16_16816(corr[nt], kF16NegMagic, kF16NegMagic, kF16NegMagic, kF16NegMagic, bf[nt][2], bf[nt][3]);
+      // A rows: low-nibble positions (k = 2c, 2c + 1) -1032, high-nibble ones -1152
+      mma_f16_16816(corr[nt], kF16NegMagic, kF16NegMagic, kF16NegMagicHi, kF16NegMagicHi, bf[nt][0], bf[nt][1]);
+      mma_f16_16816(corr[nt], kF16NegMagic, kF16NegMagic, kF16NegMagicHi, kF16NegMagicHi, bf[nt][2], bf[nt][3]);
     }
     uint32_t w[kDnM][2];
     float sc[kDnM][2];
@@ -289,8 +308,8 @@ __device__ __forceinline__ void dn_compute(uint32_t st, uint32_t hb, int cw, int
 #pragma unroll
     for (int m = 0; m < kDnM; ++m) {
       uint32_t d[4], e[4];
-      dequant_word_f16(w[m][0], d);
-      dequant_word_f16(w[m][1], e);
+      dequant_word_f16x16(w[m][0], d);
+      dequant_word_f16x16(w[m][1], e);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         float t4[4] = {corr[nt][0], corr[nt][1], corr[nt][2], corr[nt][3]};
@@ -657,7 +676,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
         const int3 u = sc.unit(ticket);
         ++P.ui;
         next = atomicAdd(a.sync + kSyncQueue, 1);  // needed at the next unit only
-        for (int ch = 0; ch < nch && ok; ++ch) ok = P.issue(2 * u.z, u.x, u.y, ch);
+        for (int ch = 0; ch < nch && ok; ++ch) {
+          ok = P.issue(2 * u.z, u.x, u.y, ch);
+          // the kernel's first stage lands before the rest of the ring is
+          // requested (all SMs ask at once; the consumers start one stage earlier)
+          if (ok && P.j == 1) ok = mbar_wait_bounded(full0, 0, a.status);
+        }
         for (int ch = 0; ch < nchd && ok; ++ch) ok = P.issue(2 * u.z + 1, u.x, u.y, ch);
         ticket = next;
       }
@@ -819,7 +843,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
                 const float gv = v[e2];
                 const float hv = gv / (1.0f + expf(-gv)) * v[2 + e2];
                 if (n < cnt && !(fabsf(hv) < 65504.f)) atomicOr(a.status, DEV_RANGE);
-                *reinterpret_cast<__half*>(hb + n * HB + 2 * col) = __float2half_rn(hv);
+                // odd rows of I meet high nibbles in the down MMA: stored as h / 16
+                *reinterpret_cast<__half*>(hb + n * HB + 2 * col) = __float2half_rn((il & 1) ? hv * 0.0625f : hv);
               }
             }
         }
