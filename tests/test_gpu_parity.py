@@ -532,3 +532,57 @@ def test_negative_control_one_corrupted_byte_fails_the_gate():
     y_bad = oracle.Layer(bad.to("cpu")).rows(ids, w, rows=hit)
     check_y(out_bad["y"][hit], y_bad, what="corrupted pool")
     assert np.array_equal(out_bad["y"][miss], out["y"][miss])
+
+
+# ---------------------------------------------------------------- more shapes and flags
+def test_prefill_without_shared_expert():
+    cfg = synth.MoeConfig("pf_noshared", H=1024, I=512, E=64, k=6, T=200, zipf_s=1.0)
+    inp = synth.make_layer(cfg, 11)
+    out, _ = run_layer(inp)
+    ids, w, we, y = oracle_layer(inp, inp.logits.numpy())
+    assert np.array_equal(out["ids"], ids)
+    assert_weights_match(out["w"], w, we)
+    check_y(out["y"], y, what="prefill without shared expert")
+
+
+def test_fp32_chunk_takes_the_separate_path_with_chunked_permutation():
+    cfg = synth.MoeConfig("f32_chunk", H=384, I=256, E=48, k=8, T=160, shared_I=128, zipf_s=1.0,
+                          x_dtype="f32")
+    assert cfg.T * cfg.k > 1024
+    inp = synth.make_layer(cfg, 12)
+    out, _ = run_layer(inp)
+    ids, w, we, y = oracle_layer(inp, inp.logits.numpy())
+    assert np.array_equal(out["ids"], ids)
+    check_y(out["y"], y, what="fp32 chunk")
+
+
+def test_fused_slot_beyond_pool_is_flagged_and_treated_as_miss():
+    cfg = synth.MoeConfig("badslot", H=1024, I=256, E=32, k=4, T=8, shared_I=256, zipf_s=1.0)
+    inp = synth.make_layer(cfg, 13)
+    ids, _, _ = oracle.route(inp.logits.numpy(), cfg.k)
+    e_bad = int(ids[0][0])
+    sm = torch.arange(cfg.E, dtype=torch.int32)
+    sm[e_bad] = cfg.E + 5  # beyond the pool's S = E slots
+    dinp = inp.to(DEV)
+    lay = MoeLayer(dinp, T_max=cfg.T)
+    out = lay.forward(dinp.logits, dinp.x, slot_map=sm.to(DEV))
+    torch.cuda.synchronize()
+    code, bits = lay.status()
+    assert bits & 2 and code == _lib.MOE_ERR_DEVICE
+    sm_ref = sm.clone()
+    sm_ref[e_bad] = -1
+    y = oracle.Layer(inp).rows(ids, oracle.route(inp.logits.numpy(), cfg.k)[1], slot_map=sm_ref.numpy())
+    check_y(out["y"].cpu().numpy(), y, what="bad slot as miss")
+    assert int(out["n_miss"].item()) >= 1
+    assert e_bad in out["miss_ids"].cpu().numpy()[:int(out["n_miss"].item())]
+
+
+@pytest.mark.parametrize("E,k", [(40, 1), (100, 3)])
+def test_fused_odd_expert_counts(E, k):
+    cfg = synth.MoeConfig("odd", H=1024, I=256, E=E, k=k, T=8, shared_I=256, zipf_s=1.0)
+    inp = synth.make_layer(cfg, 14)
+    out, _ = run_layer(inp)
+    ids, w, we, y = oracle_layer(inp, inp.logits.numpy())
+    assert np.array_equal(out["ids"], ids)
+    assert_weights_match(out["w"], w, we)
+    check_y(out["y"], y, what=f"E={E} k={k}")
