@@ -11,28 +11,31 @@
 // Two persistent kernels, one per GEMM, each a warp-specialised pipeline:
 //   warp 12 (one thread) streams a job's int4 codes and fp16 scales (TMA tensor
 //   copies, 256 columns of K per raw stage);
-//   warps 4-11 dequantise a raw stage into the job's fp16 weight tile (256
-//   rows x 64 columns of K per step, K-major, 128-byte swizzle): q = (1024 +
-//   (q ^ 8)) - 1032 exactly, then q * s with the fp16 scale, rounded once
-//   (2^-12);
+//   16 warps dequantise a raw stage, q = (1024 + (q ^ 8)) - 1032 exactly, then
+//   q * s with the fp16 scale, rounded once (2^-12): for gate/up one thread per
+//   weight row writes 64 columns of K per step into tensor memory (tcgen05.st,
+//   a ring of 4 steps; a warp reaches its TMEM lane quarter, the warps of a
+//   quarter split the gate and up matrices and the even and odd steps); for
+//   down into a shared-memory tile (256 rows x 64 columns, K-major, 128-byte
+//   swizzle);
 //   warp 13 (one thread) streams the job's token rows of the expert-sorted x
-//   or h into a 128-row tile per step (a TMA box of 16, 32, 64 or 128 rows by
-//   the job's token count; the stale rows below it only reach accumulator
-//   lanes that are never read);
+//   or h (a TMA box of 16, 32, 64 or 128 rows by the job's token count);
 //   warp 14 (the whole warp, its elected lane issuing) runs tcgen05.mma with
-//   the token tile as A (M = 128) and the weight tile as B (N = 256), K = 16,
-//   into one of two TMEM accumulators, and commits each stage back to its
-//   producers. Measured on GB300, a tcgen05.mma costs about 200 cycles of the
-//   tensor pipe in a stream with commits, whatever its N: the cost of these
-//   GEMMs is their number of MMAs, so each MMA takes the largest operand shape
-//   (tokens as M, 256 weight rows as N), half as many as with the weights as M;
-//   warps 0-3 (TMEM lanes = tokens) drain the accumulators: each thread holds
-//   one token's 256 weight rows and writes h = silu(g) u in fp16 (gate/up) or
-//   w * (W_d h) as fp32 partials (down) as contiguous rows.
+//   each 128-row weight matrix as A (gate/up: from tensor memory; down: from
+//   shared memory) and the job's tokens as B (N = tokens rounded to 16),
+//   K = 16, and commits each stage back to its producers. Keeping the gate/up
+//   weight tiles in tensor memory takes their write and read (64 KB per step)
+//   off the shared-memory port;
+//   8 epilogue warps (TMEM lanes = weight rows) drain the accumulators: each
+//   thread holds one weight row's outputs for the job's tokens and writes
+//   h = silu(g) u in fp16 (gate/up: gate and up rows meet on the same lane;
+//   one accumulator, the tensor memory beyond it holds the weight ring) or
+//   w * (W_d h) as fp32 partials (down: two accumulators in turn).
 // Both operands are fp16: the tensor cores take one type for A and B, and fp16
 // keeps q * s and h to 2^-12 where bf16 would round to 2^-9. x enters as
 // x / 2^e_t in fp16, written once per routed pair in the expert-sorted row
-// order (x16_prep_kernel; e_t is the smallest power of two that keeps the row
+// order, the columns of each group of 8 in the order (0, 4, 1, 5, 2, 6, 3, 7)
+// in which the gate/up dequantisation yields the codes (x16_prep_kernel; e_t is the smallest power of two that keeps the row
 // below 2^15, 0 for ordinary activations): exact for every bf16 value in
 // range, and the gate/up epilogue multiplies g and u back by 2^e_t.
 // A job is (active expert, 128 gate and 128 up rows, or 256 down rows, up to
@@ -55,6 +58,13 @@ namespace pf {
 constexpr int kBM = 128;              // weight rows per tile (two tiles per job)
 constexpr int kNT = 128;              // tokens per job at most (gate/up: the MMA's M; down: its N)
 constexpr int kRawSt = 2, kASt = 2, kBSt = 4;
+// gate/up: the dequantised weight tiles live in tensor memory, a ring of 4
+// steps from column kTmA on, per step two matrices of 128 lanes x 32 columns
+// (64 fp16 of K); the accumulator (gate at columns 0-127, up at 128-255) is
+// single-buffered
+constexpr int kTmA = 256, kTmAStage = 64, kTmAMat = 32, kAStTm = 4;
+template <bool GU>
+__host__ __device__ constexpr int a_stages() { return GU ? kAStTm : kASt; }
 // warps 0-3 and 15-18 epilogue, 4-11 and 19-26 dequant, 12-13 producers, 14 MMA
 constexpr int kThreads = 864;
 constexpr int kDqWarps = 16;          // 8 per weight tile: one 16-row band each
@@ -90,7 +100,7 @@ template <bool GU>
 __host__ __device__ constexpr int raw_bytes() { return nmat<GU>() * (kCodeBox + kScaleBox); }
 template <bool GU>
 __host__ __device__ constexpr size_t smem_bytes() {
-  return 1024 + (size_t)kRawSt * raw_bytes<GU>() + (size_t)kASt * nmat<GU>() * kATile +
+  return 1024 + (size_t)kRawSt * raw_bytes<GU>() + (GU ? 0 : (size_t)kASt * nmat<GU>() * kATile) +
          (size_t)kBSt * kBTile;
 }
 
@@ -122,6 +132,25 @@ __device__ __forceinline__ void tc_mma_el(uint32_t d, uint64_t ad, uint64_t bd, 
       " @q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
       "l"(ad), "l"(bd), "r"(idesc), "r"(acc), "r"(lead));
 }
+// A from tensor memory (K-major: row i in TMEM lane i, two fp16 of K per column)
+__device__ __forceinline__ void tc_mma_ts_el(uint32_t d, uint32_t at, uint64_t bd, uint32_t idesc, uint32_t acc,
+                                             uint32_t lead) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
+      "r"(at), "l"(bd), "r"(idesc), "r"(acc), "r"(lead));
+}
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tc_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tc_commit_el(uint32_t bar, uint32_t lead) {
   asm volatile(
       "{\n .reg .pred q;\n setp.ne.b32 q, %1, 0;\n"
@@ -156,6 +185,22 @@ __device__ __forceinline__ void dequant_word_h(uint32_t wd, __half2 s2, uint32_t
   }
 }
 
+// One word of codes (columns 8c..8c+7) -> four f16x2 registers of q * s in the
+// order the nibbles come out: (0, 4), (1, 5), (2, 6), (3, 7). The gate/up B
+// operand (x16) holds its columns in the same order within each group of 8.
+__device__ __forceinline__ void dequant_word_h_perm(uint32_t wd, __half2 s2, uint32_t (&o)[4]) {
+  const uint32_t mask = 0x000F000Fu, magic = 0x64086408u;  // f16 1024 + (q ^ 8) = 1032 + q
+  const uint32_t x[4] = {lop3_and_xor(wd, mask, magic), lop3_and_xor(wd >> 4, mask, magic),
+                         lop3_and_xor(wd >> 8, mask, magic), lop3_and_xor(wd >> 12, mask, magic)};
+  const __half2 m1032 = __floats2half2_rn(1032.f, 1032.f);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 v = *reinterpret_cast<const __half2*>(&x[i]);
+    v = __hmul2(__hsub2(v, m1032), s2);  // q exactly, then one rounding of q * s
+    o[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+}
+
 struct Job {
   int a, mt, n0, nn, np;   // active entry, row tile, first token slot, tokens, tokens rounded to 16
   int bsel;                // token box of 16 << bsel rows; a token slot holds 8 >> bsel boxes
@@ -167,10 +212,11 @@ template <bool GU>
 __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__ Args a) {
   constexpr int NM = nmat<GU>();
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t s_bar[2 * kRawSt + 2 * kASt + 2 * kBSt + 4];
+  __shared__ __align__(8) uint64_t s_bar[2 * kRawSt + 2 * kAStTm + 2 * kBSt + 4];
   __shared__ int s_js[kMaxAct + 1];      // first job of each active entry
   __shared__ int s_off[kMaxAct], s_cnt[kMaxAct], s_slot[kMaxAct];
   __shared__ float s_colf[2][kNT];       // down: the routing weight of each token column of a job
+  __shared__ float s_cfw[kEpiWarps][kNT];  // gate/up: each epilogue warp's token prescales
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -185,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
   const uint32_t sA = sraw + kRawSt * raw_bytes<GU>();
   const uint32_t bar0 = smem_u32(&s_bar[0]);
   const uint32_t raw_full = bar0, raw_empty = raw_full + 8 * kRawSt;
-  const uint32_t a_full = raw_empty + 8 * kRawSt, a_empty = a_full + 8 * kASt;
-  const uint32_t b_full = a_empty + 8 * kASt, b_empty = b_full + 8 * kBSt;
+  const uint32_t a_full = raw_empty + 8 * kRawSt, a_empty = a_full + 8 * kAStTm;
+  const uint32_t b_full = a_empty + 8 * kAStTm, b_empty = b_full + 8 * kBSt;
   const uint32_t acc_full = b_empty + 8 * kBSt, acc_empty = acc_full + 16;
   volatile int* abort_flag = &s_abort;
 
@@ -196,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       mbar_init(raw_full + 8 * i, 1);
       mbar_init(raw_empty + 8 * i, kDqWarps);  // one arrival per dequantising warp
     }
-    for (int i = 0; i < kASt; ++i) {
-      mbar_init(a_full + 8 * i, kDqWarps);
+    for (int i = 0; i < a_stages<GU>(); ++i) {
+      mbar_init(a_full + 8 * i, GU ? kDqWarps / 2 : kDqWarps);  // gate/up: the 8 warps of the step's parity
       mbar_init(a_empty + 8 * i, 1);
     }
     for (int i = 0; i < kBSt; ++i) {
@@ -336,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     __syncwarp();
   } else if (warp == 14) {
     // ================= MMA issuer (whole warp, elected lane issues) =================
-    // D[token][weight row] += X(128 x 16) . W(256 x 16)^T: four MMAs per step
+    // D[weight row][token] += W(128 x 16) . X(np x 16)^T per matrix: eight MMAs per step
     const uint32_t lead = elect_lane();
     // descriptors of the first tiles; the others differ by their address / 16
     // in the low field (no carry: shared addresses < 256 KB)
@@ -344,8 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     int acnt = 0, bcnt = 0, jcnt = 0;
     for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
       const Job jb = job_of(j);
-      const int ab = jcnt & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait_short(acc_empty + 8 * ab, ((jcnt >> 1) & 1) ^ 1, a.status))) {
+      const int ab = GU ? 0 : jcnt & 1;
+      const uint32_t accpar = GU ? ((jcnt & 1) ^ 1) : (((jcnt >> 1) & 1) ^ 1);
+      if (!__all_sync(0xffffffffu, mbar_wait_short(acc_empty + 8 * ab, accpar, a.status))) {
         *abort_flag = 1;
         break;
       }
@@ -353,15 +400,15 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       const int nkb = k_of(jb) / 64;
       const int spb = 8 >> jb.bsel;
       const uint32_t bbytes = (16u << jb.bsel) * 128;
-      // gate/up: tokens as A (M = 128), the 256 weight rows as B (N = 256);
-      // down: each 128-row weight tile as A, the job's tokens as B (N = np)
-      const uint32_t idesc = GU ? idesc_f16(kNT, 2 * kBM) : idesc_f16(kBM, jb.np);
+      // each 128-row weight matrix (gate/up: gate and up, from tensor memory;
+      // down: two row tiles, from shared memory) as A, the job's tokens as B
+      const uint32_t idesc = idesc_f16(kBM, jb.np);
       bool ok = true;
       for (int kb = 0, u = 0; kb < nkb; ++kb) {  // u = kb mod spb (a power of two)
-        const int as = acnt % kASt, bs = bcnt % kBSt;
+        const int as = acnt % a_stages<GU>(), bs = bcnt % kBSt;
+        const uint32_t apar = (acnt / a_stages<GU>()) & 1;
         // a ready stage is the common case: test once before the sleeping wait
-        ok = (mbar_test(a_full + 8 * as, (acnt / kASt) & 1) ||
-              mbar_wait_short(a_full + 8 * as, (acnt / kASt) & 1, a.status)) &&
+        ok = (mbar_test(a_full + 8 * as, apar) || mbar_wait_short(a_full + 8 * as, apar, a.status)) &&
              (u != 0 || mbar_test(b_full + 8 * bs, (bcnt / kBSt) & 1) ||
               mbar_wait_short(b_full + 8 * bs, (bcnt / kBSt) & 1, a.status));
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
@@ -369,10 +416,13 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
         const uint64_t xdk = xd0 + ((uint32_t)(bs * kBTile + u * bbytes) >> 4);
         const uint64_t wdk = wd0 + ((uint32_t)(as * NM * kATile) >> 4);
         if constexpr (GU) {
+          const uint32_t ta = tmem + kTmA + as * kTmAStage;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_el(tmem + ab * 256, xdk + ((kk * 32) >> 4), wdk + ((kk * 32) >> 4), idesc,
-                      (kb > 0 || kk > 0) ? 1u : 0u, lead);
+#pragma unroll
+            for (int m = 0; m < NM; ++m)  // K = 16: 8 TMEM columns of A
+              tc_mma_ts_el(tmem + m * kBM, ta + m * kTmAMat + kk * 8, xdk + ((kk * 32) >> 4), idesc,
+                           (kb > 0 || kk > 0) ? 1u : 0u, lead);
         } else {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
@@ -403,6 +453,66 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     // Thread: row r, 32-column block h of each 64-column step. The 8 lanes of a
     // quarter-warp read 8 consecutive rows of one block: 8 different 16-byte
     // chunks of the swizzled raw rows, no bank conflict.
+    if constexpr (GU) {
+    // Thread = one weight row r of matrix m, which is TMEM lane r of the A
+    // tiles (a warp reaches lane quarter warp mod 4); the warps of each quarter
+    // split the matrices and the even and odd steps. Per step of 64 columns:
+    // 32 code bytes (two 16-byte chunks of the swizzled raw row) and the scales
+    // of its two 32-column blocks, 32 registers of fp16 pairs to the step's
+    // TMEM columns.
+    const int q4 = warp & 3;
+    const int idx = warp <= 11 ? (warp - 4) >> 2 : 2 + ((warp - 19) >> 2);
+    const int m = idx & 1, par = idx >> 1;
+    const int r = 32 * q4 + lane;
+    const uint32_t rsw = (uint32_t)(r & 7);
+    const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + kTmA + m * kTmAMat;
+    int rcnt = 0, acnt = 0;
+    for (int j = bid; j < njobs && !*abort_flag; j += G) {
+      const Job jb = job_of(j);
+      const int K = k_of(jb);
+      bool ok = true;
+      for (int kr = 0; kr < K / 256 && ok; ++kr) {
+        const int rs = rcnt % kRawSt;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_short(raw_full + 8 * rs, (rcnt / kRawSt) & 1, a.status))))
+          break;
+        const uint32_t st = sraw + rs * raw_bytes<GU>();
+        const uint32_t crow = st + m * kCodeBox + r * 128;
+        const uint32_t srow = st + NM * kCodeBox + m * kScaleBox + r * 16;
+        for (int s4 = 0; s4 < 4 && ok; ++s4, ++acnt) {
+          if ((s4 & 1) != par) continue;  // the other warps of the quarter take this step
+          const int as = acnt % kAStTm;
+          if (!(ok = __all_sync(0xffffffffu,
+                                mbar_wait_short(a_empty + 8 * as, ((acnt / kAStTm) & 1) ^ 1, a.status))))
+            break;
+          tc_fence_after();
+          const uint4 c0 = ld_s128(crow + (((uint32_t)(2 * s4) ^ rsw) << 4));
+          const uint4 c1 = ld_s128(crow + (((uint32_t)(2 * s4 + 1) ^ rsw) << 4));
+          const uint32_t sc = ld_s32(srow + 4 * s4);  // blocks 2 s4 (low half) and 2 s4 + 1
+          const uint32_t s0u = prmt(sc, 0u, 0x1010), s1u = prmt(sc, 0u, 0x3232);
+          const __half2 s0 = *reinterpret_cast<const __half2*>(&s0u);
+          const __half2 s1 = *reinterpret_cast<const __half2*>(&s1u);
+          uint32_t o[8][4];
+          dequant_word_h_perm(c0.x, s0, o[0]);
+          dequant_word_h_perm(c0.y, s0, o[1]);
+          dequant_word_h_perm(c0.z, s0, o[2]);
+          dequant_word_h_perm(c0.w, s0, o[3]);
+          dequant_word_h_perm(c1.x, s1, o[4]);
+          dequant_word_h_perm(c1.y, s1, o[5]);
+          dequant_word_h_perm(c1.z, s1, o[6]);
+          dequant_word_h_perm(c1.w, s1, o[7]);
+          tc_st32(trow + as * kTmAStage, *reinterpret_cast<const uint32_t(*)[32]>(&o[0][0]));
+          tc_st_wait();
+          tc_fence_before();  // the MMA warp reads the tile after the barrier
+          __syncwarp();
+          if (lane == 0) mbar_arrive(a_full + 8 * as);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(raw_empty + 8 * rs);
+        ++rcnt;
+      }
+      if (!ok) *abort_flag = 1;
+    }
+    } else {
     const int wd = warp <= 11 ? warp - 4 : warp - 11, m = wd >> 3;
     const int h = lane >> 4;
     const int r = (wd & 7) * 16 + (lane & 15);
@@ -446,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       }
       if (!ok) *abort_flag = 1;
     }
+    }
   } else {
     // ================= epilogue (warps 0-3 and 15-18) =================
     // A warp reaches the TMEM lane quarter warp mod 4; the two warps of a
@@ -454,56 +565,52 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     const int qw = warp & 3, half = warp >= 15 ? 1 : 0;
     int jcnt = 0;
     if constexpr (GU) {
-    // Gate/up: thread = one token of the job (TMEM lane); its accumulator row
-    // holds the 128 gate rows at columns 0-127 and the same up rows at 128-255,
-    // and h goes out as a contiguous fp16 row segment.
-    const int t = qw * 32 + lane;
+    // Gate/up: thread = one intermediate row of the job's 128 (TMEM lane); the
+    // columns are the job's tokens, gate at 0 and up at 128. The two warps of
+    // a quarter take alternate 16-token chunks; each warp store is 32
+    // consecutive fp16 of one token's h row.
+    const int row = qw * 32 + lane;
     for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
       const Job jb = job_of(j);
-      const int ab = jcnt & 1;
-      const bool valid = t < jb.nn;
-      const size_t s = (size_t)jb.off + jb.n0 + (valid ? t : 0);  // the token's expert-sorted row
-      // the token's x prescale, fetched while the job's MMAs run
-      const float cf = !valid ? 0.f : jb.sh ? __ldg(a.xscale + (s - P)) : __ldg(a.xscale + a.sorted_pair[s] / a.k);
-      if (!__all_sync(0xffffffffu, mbar_wait_short(acc_full + 8 * ab, (jcnt >> 1) & 1, a.status))) {
+      // the x prescale of each token column (this warp's own copy: no barrier
+      // with the other epilogue warps), fetched while the job's MMAs run
+      float* colf = s_cfw[qw + 4 * half];
+      __syncwarp();  // the previous job's reads of colf are done
+      for (int e = lane; e < jb.nn; e += 32) {
+        const size_t s = (size_t)jb.off + jb.n0 + e;
+        colf[e] = jb.sh ? __ldg(a.xscale + (s - P)) : __ldg(a.xscale + a.sorted_pair[s] / a.k);
+      }
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, mbar_wait_short(acc_full, jcnt & 1, a.status))) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      if (qw * 32 < jb.nn) {  // warp-uniform: a warp with no token of the job reads nothing
-        const uint32_t tb = tmem + ((uint32_t)(qw * 32) << 16) + ab * 256;
-        bool range_ok = true;
-        uint16_t* hp = a.h + s * a.Imax + jb.mt * kBM;
+      const uint32_t tb = tmem + ((uint32_t)(qw * 32) << 16);
+      bool range_ok = true;
+      uint16_t* hcol = a.h + (size_t)(jb.off + jb.n0) * a.Imax + jb.mt * kBM + row;
 #pragma unroll 1
-        for (int c0 = half * (kBM / 2); c0 < (half + 1) * (kBM / 2); c0 += 16) {
-          uint32_t g[16], u[16];
-          tc_ld16(tb + c0, g);
-          tc_ld16(tb + kBM + c0, u);
-          tc_ld_wait();
-          uint32_t hv2[8];
+      for (int c0 = half * 16; c0 < jb.np; c0 += 32) {
+        uint32_t g[16], u[16];
+        tc_ld16(tb + c0, g);
+        tc_ld16(tb + kBM + c0, u);
+        tc_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float hv[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {  // undo the token's power-of-two prescale of x (exact)
-              const float gv = __uint_as_float(g[2 * i + e]) * cf, uv = __uint_as_float(u[2 * i + e]) * cf;
-              hv[e] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;  // rounded to fp16 below
-              range_ok = range_ok && (!valid || fabsf(hv[e]) < 65504.f);
-            }
-            const __half2 h2 = __floats2half2_rn(hv[0], hv[1]);
-            hv2[i] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(hp + c0);
-            d4[0] = make_uint4(hv2[0], hv2[1], hv2[2], hv2[3]);
-            d4[1] = make_uint4(hv2[4], hv2[5], hv2[6], hv2[7]);
+        for (int i = 0; i < 16; ++i) {
+          const int c = c0 + i;
+          if (c < jb.nn) {  // undo the token's power-of-two prescale of x (exact)
+            const float cf = colf[c];
+            const float gv = __uint_as_float(g[i]) * cf, uv = __uint_as_float(u[i]) * cf;
+            const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;  // rounded to fp16 below
+            range_ok = range_ok && fabsf(hv) < 65504.f;
+            hcol[(size_t)c * a.Imax] = __half_as_ushort(__float2half_rn(hv));
           }
         }
-        if (!range_ok) atomicOr(a.status, DEV_RANGE);
       }
+      if (!range_ok) atomicOr(a.status, DEV_RANGE);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty + 8 * ab);
+      if (lane == 0) mbar_arrive(acc_empty);
     }
     } else {
     // Down: thread = one output row of weight tile `half` (TMEM lane), the
@@ -576,10 +683,14 @@ __global__ void __launch_bounds__(256) x16_prep_kernel(const uint16_t* __restric
   for (int i = threadIdx.x * 8; i < H; i += 256 * 8) {  // 8 columns (16 bytes) per thread and step
     const uint4 v = *reinterpret_cast<const uint4*>(xr + i);
     const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    // columns (q, q + 4) of the group of 8 in register q, the order of the
+    // gate/up dequantisation's nibble pairs
     uint32_t o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float lo = __uint_as_float(in[q] << 16) * inv, hi = __uint_as_float(in[q] & 0xFFFF0000u) * inv;
+      const uint32_t a0 = in[q >> 1], a1 = in[(q >> 1) + 2];
+      const float lo = __uint_as_float((q & 1) ? (a0 & 0xFFFF0000u) : (a0 << 16)) * inv;
+      const float hi = __uint_as_float((q & 1) ? (a1 & 0xFFFF0000u) : (a1 << 16)) * inv;
       const __half2 h2 = __floats2half2_rn(lo, hi);
       o[q] = *reinterpret_cast<const uint32_t*>(&h2);
     }
