@@ -12,25 +12,26 @@
 //   warp 12 (one thread) streams a job's int4 codes and fp16 scales (TMA tensor
 //   copies, 256 columns of K per raw stage);
 //   16 warps dequantise a raw stage, q = (1024 + (q ^ 8)) - 1032 exactly, then
-//   q * s with the fp16 scale, rounded once (2^-12): for gate/up one thread per
-//   weight row writes 64 columns of K per step into tensor memory (tcgen05.st,
-//   a ring of 4 steps; a warp reaches its TMEM lane quarter, the warps of a
-//   quarter split the gate and up matrices and the even and odd steps); for
-//   down into a shared-memory tile (256 rows x 64 columns, K-major, 128-byte
-//   swizzle);
+//   q * s with the fp16 scale, rounded once (2^-12): one thread per weight row
+//   writes 64 columns of K per step into tensor memory (tcgen05.st, a ring of
+//   4 steps; a warp reaches its TMEM lane quarter, the warps of a quarter split
+//   the two matrices of a job (gate and up, or two down row tiles) and the
+//   even and odd steps);
 //   warp 13 (one thread) streams the job's token rows of the expert-sorted x
 //   or h (a TMA box of 16, 32, 64 or 128 rows by the job's token count);
 //   warp 14 (the whole warp, its elected lane issuing) runs tcgen05.mma with
-//   each 128-row weight matrix as A (gate/up: from tensor memory; down: from
-//   shared memory) and the job's tokens as B (N = tokens rounded to 16),
-//   K = 16, and commits each stage back to its producers. Keeping the gate/up
-//   weight tiles in tensor memory takes their write and read (64 KB per step)
-//   off the shared-memory port;
+//   each 128-row weight matrix as A, from tensor memory, and the job's tokens
+//   as B (N = tokens rounded to 16), K = 16, and commits each stage back to its
+//   producers. Keeping the weight tiles in tensor memory takes their write and
+//   read (64 KB per step) off the shared-memory port;
 //   8 epilogue warps (TMEM lanes = weight rows) drain the accumulators: each
 //   thread holds one weight row's outputs for the job's tokens and writes
 //   h = silu(g) u in fp16 (gate/up: gate and up rows meet on the same lane;
-//   one accumulator, the tensor memory beyond it holds the weight ring) or
-//   w * (W_d h) as fp32 partials (down: two accumulators in turn).
+//   one accumulator, jobs of up to 128 tokens) or w * (W_d h) as fp32
+//   partials (down: two accumulators in turn, jobs of up to 64 tokens); the
+//   weight ring takes the tensor memory's other 256 columns. h is stored with
+//   the columns of each group of 8 in the order (0, 4, 1, 5, 2, 6, 3, 7), the
+//   order in which the down dequantisation yields the codes.
 // Both operands are fp16: the tensor cores take one type for A and B, and fp16
 // keeps q * s and h to 2^-12 where bf16 would round to 2^-9. x enters as
 // x / 2^e_t in fp16, written once per routed pair in the expert-sorted row
@@ -56,15 +57,19 @@ namespace moe {
 namespace pf {
 
 constexpr int kBM = 128;              // weight rows per tile (two tiles per job)
-constexpr int kNT = 128;              // tokens per job at most (gate/up: the MMA's M; down: its N)
-constexpr int kRawSt = 2, kASt = 2, kBSt = 4;
-// gate/up: the dequantised weight tiles live in tensor memory, a ring of 4
-// steps from column kTmA on, per step two matrices of 128 lanes x 32 columns
-// (64 fp16 of K); the accumulator (gate at columns 0-127, up at 128-255) is
-// single-buffered
+constexpr int kNT = 128;              // tokens per gate/up job at most (the MMA's N); down: 64
+constexpr int kRawSt = 2, kBSt = 4;
+// The dequantised weight tiles live in tensor memory, a ring of 4 steps from
+// column kTmA on, per step two matrices of 128 lanes x 32 columns (64 fp16 of
+// K). Columns 0-255: gate/up one accumulator (gate at 0, up at 128); down two
+// (at 0 and 128), each holding its two row tiles at +0 and +64.
 constexpr int kTmA = 256, kTmAStage = 64, kTmAMat = 32, kAStTm = 4;
 template <bool GU>
-__host__ __device__ constexpr int a_stages() { return GU ? kAStTm : kASt; }
+__host__ __device__ constexpr int a_stages() { return kAStTm; }
+// tokens per job at most: gate/up 128 (one accumulator of 256 columns), down 64
+// (two accumulators of two 64-column row tiles)
+template <bool GU>
+__host__ __device__ constexpr int job_nt() { return GU ? kNT : kNT / 2; }
 // warps 0-3 and 15-18 epilogue, 4-11 and 19-26 dequant, 12-13 producers, 14 MMA
 constexpr int kThreads = 864;
 constexpr int kDqWarps = 16;          // 8 per weight tile: one 16-row band each
@@ -72,7 +77,6 @@ constexpr int kEpiWarps = 8;          // two per TMEM lane quarter, each for hal
 constexpr int kMaxAct = kMaxE + 1;
 constexpr int kCodeBox = 128 * 128;   // one raw code box: 128 rows x 128 bytes (256 columns)
 constexpr int kScaleBox = 128 * 16;   // one raw scale box: 128 rows x 8 fp16
-constexpr int kATile = 128 * 128;     // one fp16 weight tile: 128 rows x 64 columns (two per step)
 constexpr int kBTile = kNT * 128;     // one fp16 token tile: 128 rows x 64 columns
 
 struct Args {
@@ -100,8 +104,7 @@ template <bool GU>
 __host__ __device__ constexpr int raw_bytes() { return nmat<GU>() * (kCodeBox + kScaleBox); }
 template <bool GU>
 __host__ __device__ constexpr size_t smem_bytes() {
-  return 1024 + (size_t)kRawSt * raw_bytes<GU>() + (GU ? 0 : (size_t)kASt * nmat<GU>() * kATile) +
-         (size_t)kBSt * kBTile;
+  return 1024 + (size_t)kRawSt * raw_bytes<GU>() + (size_t)kBSt * kBTile;
 }
 
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       mbar_init(raw_empty + 8 * i, kDqWarps);  // one arrival per dequantising warp
     }
     for (int i = 0; i < a_stages<GU>(); ++i) {
-      mbar_init(a_full + 8 * i, GU ? kDqWarps / 2 : kDqWarps);  // gate/up: the 8 warps of the step's parity
+      mbar_init(a_full + 8 * i, kDqWarps / 2);  // the 8 dequantising warps of the step's parity
       mbar_init(a_empty + 8 * i, 1);
     }
     for (int i = 0; i < kBSt; ++i) {
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     int sum = 0;
     for (int i = i0; i < i1; ++i) {
       const int rows = GU ? (s_slot[i] < 0 ? a.shI : a.I) : a.H;
-      sum += (rows / job_rows<GU>()) * ((s_cnt[i] + kNT - 1) / kNT);
+      sum += (rows / job_rows<GU>()) * ((s_cnt[i] + job_nt<GU>() - 1) / job_nt<GU>());
     }
     int x = sum;
 #pragma unroll
@@ -287,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     for (int i = i0; i < i1; ++i) {
       s_js[i] = run;
       const int rows = GU ? (s_slot[i] < 0 ? a.shI : a.I) : a.H;
-      run += (rows / job_rows<GU>()) * ((s_cnt[i] + kNT - 1) / kNT);
+      run += (rows / job_rows<GU>()) * ((s_cnt[i] + job_nt<GU>() - 1) / job_nt<GU>());
     }
     if (lane == 31) s_js[n_act] = x;
   }
@@ -311,8 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     const int nM = rows / job_rows<GU>();
     const int loc = j - s_js[lo];
     jb.mt = loc % nM;
-    jb.n0 = (loc / nM) * kNT;
-    jb.nn = min(kNT, s_cnt[lo] - jb.n0);
+    jb.n0 = (loc / nM) * job_nt<GU>();
+    jb.nn = min(job_nt<GU>(), s_cnt[lo] - jb.n0);
     jb.np = (jb.nn + 15) & ~15;
     jb.bsel = jb.np <= 16 ? 0 : jb.np <= 32 ? 1 : jb.np <= 64 ? 2 : 3;
     jb.off = s_off[lo];
@@ -386,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     const uint32_t lead = elect_lane();
     // descriptors of the first tiles; the others differ by their address / 16
     // in the low field (no carry: shared addresses < 256 KB)
-    const uint64_t xd0 = sdesc_sw128(sB), wd0 = sdesc_sw128(sA);
+    const uint64_t xd0 = sdesc_sw128(sB);
     int acnt = 0, bcnt = 0, jcnt = 0;
     for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
       const Job jb = job_of(j);
@@ -414,7 +417,6 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
         tc_fence_after();
         const uint64_t xdk = xd0 + ((uint32_t)(bs * kBTile + u * bbytes) >> 4);
-        const uint64_t wdk = wd0 + ((uint32_t)(as * NM * kATile) >> 4);
         if constexpr (GU) {
           const uint32_t ta = tmem + kTmA + as * kTmAStage;
 #pragma unroll
@@ -424,12 +426,13 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
               tc_mma_ts_el(tmem + m * kBM, ta + m * kTmAMat + kk * 8, xdk + ((kk * 32) >> 4), idesc,
                            (kb > 0 || kk > 0) ? 1u : 0u, lead);
         } else {
+          const uint32_t ta = tmem + kTmA + as * kTmAStage;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-            for (int m = 0; m < NM; ++m)
-              tc_mma_el(tmem + ab * 256 + m * 128, wdk + ((m * kATile + kk * 32) >> 4), xdk + ((kk * 32) >> 4),
-                        idesc, (kb > 0 || kk > 0) ? 1u : 0u, lead);
+            for (int m = 0; m < NM; ++m)  // accumulator ab: row tile m at 64 m
+              tc_mma_ts_el(tmem + ab * 128 + m * 64, ta + m * kTmAMat + kk * 8, xdk + ((kk * 32) >> 4), idesc,
+                           (kb > 0 || kk > 0) ? 1u : 0u, lead);
         }
         tc_commit_el(a_empty + 8 * as, lead);  // the tiles are free once these MMAs are done
         ++acnt;
@@ -453,8 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     // Thread: row r, 32-column block h of each 64-column step. The 8 lanes of a
     // quarter-warp read 8 consecutive rows of one block: 8 different 16-byte
     // chunks of the swizzled raw rows, no bank conflict.
-    if constexpr (GU) {
-    // Thread = one weight row r of matrix m, which is TMEM lane r of the A
+    {
+    // Thread = one weight row r of matrix m (gate/up: gate or up; down: row tile), which is TMEM lane r of the A
     // tiles (a warp reaches lane quarter warp mod 4); the warps of each quarter
     // split the matrices and the even and odd steps. Per step of 64 columns:
     // 32 code bytes (two 16-byte chunks of the swizzled raw row) and the scales
@@ -512,50 +515,6 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       }
       if (!ok) *abort_flag = 1;
     }
-    } else {
-    const int wd = warp <= 11 ? warp - 4 : warp - 11, m = wd >> 3;
-    const int h = lane >> 4;
-    const int r = (wd & 7) * 16 + (lane & 15);
-    int rcnt = 0, acnt = 0;
-    for (int j = bid; j < njobs && !*abort_flag; j += G) {
-      const Job jb = job_of(j);
-      const int K = k_of(jb);
-      bool ok = true;
-      for (int kr = 0; kr < K / 256 && ok; ++kr) {
-        const int rs = rcnt % kRawSt;
-        if (!(ok = mbar_wait_short(raw_full + 8 * rs, (rcnt / kRawSt) & 1, a.status))) break;
-        const uint32_t st = sraw + rs * raw_bytes<GU>();
-        for (int s4 = 0; s4 < 4 && ok; ++s4) {
-          const int as = acnt % kASt;
-          if (!(ok = mbar_wait_short(a_empty + 8 * as, ((acnt / kASt) & 1) ^ 1, a.status))) break;
-          const int c = 2 * s4 + h;  // 32-column block of the raw stage
-          {
-              const uint4 cw = ld_s128(st + m * kCodeBox + r * 128 + ((c ^ (r & 7)) << 4));
-              const uint32_t sh = ld_s32(st + NM * kCodeBox + m * kScaleBox + r * 16 + (c & ~1) * 2);
-              const uint32_t s1 = (c & 1) ? (sh >> 16) : (sh & 0xFFFFu);
-              const uint32_t s2u = s1 | (s1 << 16);
-              const __half2 s2 = *reinterpret_cast<const __half2*>(&s2u);
-              uint32_t o[4][4];
-              dequant_word_h(cw.x, s2, o[0]);
-              dequant_word_h(cw.y, s2, o[1]);
-              dequant_word_h(cw.z, s2, o[2]);
-              dequant_word_h(cw.w, s2, o[3]);
-              const uint32_t at = sA + (as * NM + m) * kATile + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                st_s128(at + ((((h << 2) + i) ^ (r & 7)) << 4), o[i][0], o[i][1], o[i][2], o[i][3]);
-            }
-          fence_proxy_async_shared();  // the MMA reads the tile through the async proxy
-          __syncwarp();
-          if (lane == 0) mbar_arrive(a_full + 8 * as);
-          ++acnt;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(raw_empty + 8 * rs);
-        ++rcnt;
-      }
-      if (!ok) *abort_flag = 1;
-    }
     }
   } else {
     // ================= epilogue (warps 0-3 and 15-18) =================
@@ -588,7 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       tc_fence_after();
       const uint32_t tb = tmem + ((uint32_t)(qw * 32) << 16);
       bool range_ok = true;
-      uint16_t* hcol = a.h + (size_t)(jb.off + jb.n0) * a.Imax + jb.mt * kBM + row;
+      // the columns of h in each group of 8 in the order (0, 4, 1, 5, 2, 6, 3, 7),
+      // the order in which the down dequantisation yields the codes
+      uint16_t* hcol = a.h + (size_t)(jb.off + jb.n0) * a.Imax + jb.mt * kBM + (row & ~7) + perm8_pos(row & 7);
 #pragma unroll 1
       for (int c0 = half * 16; c0 < jb.np; c0 += 32) {
         uint32_t g[16], u[16];
@@ -630,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
         break;
       }
       tc_fence_after();
-      const uint32_t tb = tmem + ((uint32_t)(qw * 32) << 16) + ab * 256 + half * kBM;
+      const uint32_t tb = tmem + ((uint32_t)(qw * 32) << 16) + ab * 128 + half * 64;
       float* pcol = a.partial + (size_t)(jb.off + jb.n0) * a.H + jb.mt * (2 * kBM) + half * kBM + row;
       for (int c0 = 0; c0 < jb.np; c0 += 16) {
         uint32_t v[16];
