@@ -27,7 +27,8 @@
 //   8 epilogue warps (TMEM lanes = weight rows) drain the accumulators: each
 //   thread holds one weight row's outputs for the job's tokens and writes
 //   h = silu(g) u in fp16 (gate/up: gate and up rows meet on the same lane;
-//   one accumulator, jobs of up to 128 tokens) or w * (W_d h) as fp32
+//   jobs of up to 128 tokens, those of up to 64 in alternating accumulators)
+//   or w * (W_d h) as fp32
 //   partials (down: two accumulators in turn, jobs of up to 64 tokens); the
 //   weight ring takes the tensor memory's other 256 columns. h is stored with
 //   the columns of each group of 8 in the order (0, 4, 1, 5, 2, 6, 3, 7), the
@@ -61,8 +62,10 @@ constexpr int kNT = 128;              // tokens per gate/up job at most (the MMA
 constexpr int kRawSt = 2, kBSt = 4;
 // The dequantised weight tiles live in tensor memory, a ring of 4 steps from
 // column kTmA on, per step two matrices of 128 lanes x 32 columns (64 fp16 of
-// K). Columns 0-255: gate/up one accumulator (gate at 0, up at 128); down two
-// (at 0 and 128), each holding its two row tiles at +0 and +64.
+// K). Columns 0-255: gate/up two accumulator buffers of 128 columns, a job of
+// up to 64 tokens taking one (gate at +0, up at +64) and a larger job both
+// (gate at 0, up at 128); down two (at 0 and 128), each holding its two row
+// tiles at +0 and +64.
 constexpr int kTmA = 256, kTmAStage = 64, kTmAMat = 32, kAStTm = 4;
 template <bool GU>
 __host__ __device__ constexpr int a_stages() { return kAStTm; }
@@ -203,6 +206,32 @@ __device__ __forceinline__ void dequant_word_h_perm(uint32_t wd, __half2 s2, uin
     o[i] = *reinterpret_cast<const uint32_t*>(&v);
   }
 }
+
+// Gate/up accumulators: two buffers of 128 TMEM columns. A job of up to 64
+// tokens takes one (gate at +0, up at +64), buffers in turn by small-job count;
+// a job of more tokens takes both (gate at 0, up at 128). The MMA warp and the
+// epilogue walk the same job sequence and keep the same use counts per buffer.
+struct AccUse {
+  int nsmall;   // small jobs so far
+  int u0, u1;   // uses of buffers 0 and 1 so far
+  __device__ int use(int b) const { return b ? u1 : u0; }
+  __device__ void used(int b) {
+    if (b) ++u1;
+    else ++u0;
+  }
+  __device__ void next(int np, int& b0, int& b1, uint32_t& gbase, uint32_t& uoff) {
+    if (np <= 64) {
+      b0 = b1 = nsmall++ & 1;
+      gbase = 128u * (uint32_t)b0;
+      uoff = 64;
+    } else {
+      b0 = 0;
+      b1 = 1;
+      gbase = 0;
+      uoff = 128;
+    }
+  }
+};
 
 struct Job {
   int a, mt, n0, nn, np;   // active entry, row tile, first token slot, tokens, tokens rounded to 16
@@ -391,11 +420,21 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     // in the low field (no carry: shared addresses < 256 KB)
     const uint64_t xd0 = sdesc_sw128(sB);
     int acnt = 0, bcnt = 0, jcnt = 0;
+    AccUse au{0, 0, 0};
     for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
       const Job jb = job_of(j);
       const int ab = GU ? 0 : jcnt & 1;
-      const uint32_t accpar = GU ? ((jcnt & 1) ^ 1) : (((jcnt >> 1) & 1) ^ 1);
-      if (!__all_sync(0xffffffffu, mbar_wait_short(acc_empty + 8 * ab, accpar, a.status))) {
+      int gb0 = 0, gb1 = 0;
+      uint32_t gbase = 0, uoff = 128;
+      bool accok;
+      if constexpr (GU) {
+        au.next(jb.np, gb0, gb1, gbase, uoff);
+        accok = mbar_wait_short(acc_empty + 8 * gb0, (au.use(gb0) & 1) ^ 1, a.status) &&
+                (gb1 == gb0 || mbar_wait_short(acc_empty + 8 * gb1, (au.use(gb1) & 1) ^ 1, a.status));
+      } else {
+        accok = mbar_wait_short(acc_empty + 8 * ab, ((jcnt >> 1) & 1) ^ 1, a.status);
+      }
+      if (!__all_sync(0xffffffffu, accok)) {
         *abort_flag = 1;
         break;
       }
@@ -423,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
           for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
             for (int m = 0; m < NM; ++m)  // K = 16: 8 TMEM columns of A
-              tc_mma_ts_el(tmem + m * kBM, ta + m * kTmAMat + kk * 8, xdk + ((kk * 32) >> 4), idesc,
+              tc_mma_ts_el(tmem + gbase + m * uoff, ta + m * kTmAMat + kk * 8, xdk + ((kk * 32) >> 4), idesc,
                            (kb > 0 || kk > 0) ? 1u : 0u, lead);
         } else {
           const uint32_t ta = tmem + kTmA + as * kTmAStage;
@@ -448,7 +487,17 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
         *abort_flag = 1;
         break;
       }
-      tc_commit_el(acc_full + 8 * ab, lead);  // the job's accumulators are complete
+      // the job's accumulators are complete
+      if constexpr (GU) {
+        tc_commit_el(acc_full + 8 * gb0, lead);
+        au.used(gb0);
+        if (gb1 != gb0) {
+          tc_commit_el(acc_full + 8 * gb1, lead);
+          au.used(gb1);
+        }
+      } else {
+        tc_commit_el(acc_full + 8 * ab, lead);
+      }
     }
     __syncwarp();
   } else if ((warp >= 4 && warp <= 11) || warp >= 19) {
@@ -529,8 +578,12 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     // a quarter take alternate 16-token chunks; each warp store is 32
     // consecutive fp16 of one token's h row.
     const int row = qw * 32 + lane;
+    AccUse au{0, 0, 0};
     for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
       const Job jb = job_of(j);
+      int gb0, gb1;
+      uint32_t gbase, uoff;
+      au.next(jb.np, gb0, gb1, gbase, uoff);
       // the x prescale of each token column (this warp's own copy: no barrier
       // with the other epilogue warps), fetched while the job's MMAs run
       float* colf = s_cfw[qw + 4 * half];
@@ -540,12 +593,14 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
         colf[e] = jb.sh ? __ldg(a.xscale + (s - P)) : __ldg(a.xscale + a.sorted_pair[s] / a.k);
       }
       __syncwarp();
-      if (!__all_sync(0xffffffffu, mbar_wait_short(acc_full, jcnt & 1, a.status))) {
+      const bool fok = mbar_wait_short(acc_full + 8 * gb0, au.use(gb0) & 1, a.status) &&
+                       (gb1 == gb0 || mbar_wait_short(acc_full + 8 * gb1, au.use(gb1) & 1, a.status));
+      if (!__all_sync(0xffffffffu, fok)) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t tb = tmem + ((uint32_t)(qw * 32) << 16);
+      const uint32_t tb = tmem + ((uint32_t)(qw * 32) << 16) + gbase;
       bool range_ok = true;
       // the columns of h in each group of 8 in the order (0, 4, 1, 5, 2, 6, 3, 7),
       // the order in which the down dequantisation yields the codes
@@ -554,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       for (int c0 = half * 16; c0 < jb.np; c0 += 32) {
         uint32_t g[16], u[16];
         tc_ld16(tb + c0, g);
-        tc_ld16(tb + kBM + c0, u);
+        tc_ld16(tb + uoff + c0, u);
         tc_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -571,7 +626,12 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
       if (!range_ok) atomicOr(a.status, DEV_RANGE);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
+      if (lane == 0) {
+        mbar_arrive(acc_empty + 8 * gb0);
+        if (gb1 != gb0) mbar_arrive(acc_empty + 8 * gb1);
+      }
+      au.used(gb0);
+      if (gb1 != gb0) au.used(gb1);
     }
     } else {
     // Down: thread = one output row of weight tile `half` (TMEM lane), the
