@@ -41,9 +41,10 @@
 // below 2^15, 0 for ordinary activations): exact for every bf16 value in
 // range, and the gate/up epilogue multiplies g and u back by 2^e_t.
 // A job is (active expert, 128 gate and 128 up rows, or 256 down rows, up to
-// 128 of its tokens); CTA b
-// takes jobs b, b + G, ... of the list both kernels derive from the
-// permutation. The ordered combine (moe_decode.cu) then sums the partials in
+// 128 of its tokens); both kernels derive the job list from the permutation,
+// large token blocks first, and each CTA takes every G-th position of it
+// (gate/up: in alternating directions), no CTA waiting for another. The
+// ordered combine (moe_decode.cu) then sums the partials in
 // j order and adds the shared expert, which enters as one more expert with all
 // T tokens.
 #include <cuda.h>
@@ -78,6 +79,7 @@ constexpr int kThreads = 864;
 constexpr int kDqWarps = 16;          // 8 per weight tile: one 16-row band each
 constexpr int kEpiWarps = 8;          // two per TMEM lane quarter, each for half of the weight rows
 constexpr int kMaxAct = kMaxE + 1;
+constexpr int kJobCap = 64;           // jobs per CTA decoded at the start (later ones on the fly)
 constexpr int kCodeBox = 128 * 128;   // one raw code box: 128 rows x 128 bytes (256 columns)
 constexpr int kScaleBox = 128 * 16;   // one raw scale box: 128 rows x 8 fp16
 constexpr int kBTile = kNT * 128;     // one fp16 token tile: 128 rows x 64 columns
@@ -234,7 +236,7 @@ struct AccUse {
 };
 
 struct Job {
-  int a, mt, n0, nn, np;   // active entry, row tile, first token slot, tokens, tokens rounded to 16
+  int mt, n0, nn, np;      // row tile, first token slot, tokens, tokens rounded to 16
   int bsel;                // token box of 16 << bsel rows; a token slot holds 8 >> bsel boxes
   int off, slot;           // first sorted row of the expert; pool slot (-1: shared)
   bool sh;
@@ -245,7 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
   constexpr int NM = nmat<GU>();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t s_bar[2 * kRawSt + 2 * kAStTm + 2 * kBSt + 4];
-  __shared__ int s_js[kMaxAct + 1];      // first job of each active entry
+  __shared__ int s_js[2][kMaxAct + 1];   // first job of each active entry, per job class
+  __shared__ int4 s_job[kJobCap];        // the CTA's first kJobCap jobs, decoded once
   __shared__ int s_off[kMaxAct], s_cnt[kMaxAct], s_slot[kMaxAct];
   __shared__ float s_colf[2][kNT];       // down: the routing weight of each token column of a job
   __shared__ float s_cfw[kEpiWarps][kNT];  // gate/up: each epilogue warp's token prescales
@@ -302,13 +305,21 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     s_slot[i] = e.slot;
   }
   __syncthreads();
-  if (warp == 0) {
+  // Two job classes: token blocks of more than half the job size (the full
+  // blocks of an entry and a large last block), then the small last blocks,
+  // each class in entry order; per entry and class, the row tiles of one token
+  // block are consecutive. The large jobs, which take longer, come first.
+  if (warp < 2) {
+    const int cls = warp;
     const int per = (n_act + 31) / 32, i0 = lane * per, i1 = min(n_act, i0 + per);
-    int sum = 0;
-    for (int i = i0; i < i1; ++i) {
+    auto njob = [&](int i) {
       const int rows = GU ? (s_slot[i] < 0 ? a.shI : a.I) : a.H;
-      sum += (rows / job_rows<GU>()) * ((s_cnt[i] + job_nt<GU>() - 1) / job_nt<GU>());
-    }
+      const int nt = job_nt<GU>(), rem = s_cnt[i] % nt;
+      const int nb = cls == 0 ? s_cnt[i] / nt + (rem > nt / 2 ? 1 : 0) : (rem > 0 && rem <= nt / 2 ? 1 : 0);
+      return (rows / job_rows<GU>()) * nb;
+    };
+    int sum = 0;
+    for (int i = i0; i < i1; ++i) sum += njob(i);
     int x = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -317,33 +328,40 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     }
     int run = x - sum;
     for (int i = i0; i < i1; ++i) {
-      s_js[i] = run;
-      const int rows = GU ? (s_slot[i] < 0 ? a.shI : a.I) : a.H;
-      run += (rows / job_rows<GU>()) * ((s_cnt[i] + job_nt<GU>() - 1) / job_nt<GU>());
+      s_js[cls][i] = run;
+      run += njob(i);
     }
-    if (lane == 31) s_js[n_act] = x;
+    if (lane == 31) s_js[cls][n_act] = x;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const int njobs = s_js[n_act];
+  const int nfirst = s_js[0][n_act];
+  const int njobs = nfirst + s_js[1][n_act];
+  // CTA b's jobs: gate/up takes list positions b, 2G - 1 - b, 2G + b,
+  // 4G - 1 - b, ... (each round of G positions in the opposite CTA order to the
+  // one before), down positions b, b + G, b + 2G, ... (measured on GB300: the
+  // order of least time for each kernel)
+  auto next_pos = [&](int j) { return GU ? j + 2 * G - 1 - 2 * (j % G) : j + G; };
 
   auto job_of = [&](int j) {
-    int lo = 0, hi = n_act - 1;  // last entry with s_js <= j
+    const int cls = j < nfirst ? 0 : 1;
+    if (cls) j -= nfirst;
+    const int* js = s_js[cls];
+    int lo = 0, hi = n_act - 1;  // last entry with js <= j
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (s_js[mid] <= j) lo = mid;
+      if (js[mid] <= j) lo = mid;
       else hi = mid - 1;
     }
     Job jb;
-    jb.a = lo;
     jb.sh = s_slot[lo] < 0;
     const int rows = GU ? (jb.sh ? a.shI : a.I) : a.H;
     const int nM = rows / job_rows<GU>();
-    const int loc = j - s_js[lo];
+    const int loc = j - js[lo];
     jb.mt = loc % nM;
-    jb.n0 = (loc / nM) * job_nt<GU>();
+    jb.n0 = (cls == 0 ? loc / nM : s_cnt[lo] / job_nt<GU>()) * job_nt<GU>();
     jb.nn = min(job_nt<GU>(), s_cnt[lo] - jb.n0);
     jb.np = (jb.nn + 15) & ~15;
     jb.bsel = jb.np <= 16 ? 0 : jb.np <= 32 ? 1 : jb.np <= 64 ? 2 : 3;
@@ -352,13 +370,40 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     return jb;
   };
   auto k_of = [&](const Job& jb) { return GU ? a.H : (jb.sh ? a.shI : a.I); };
+  // The CTA's i-th job: from the table decoded below for i < kJobCap (every
+  // role walks the same sequence; one decode instead of one per warp)
+  auto job_at = [&](int i, int j) {
+    if (i >= kJobCap) return job_of(j);
+    const int4 v = s_job[i];
+    Job jb;
+    jb.off = v.x;
+    jb.slot = v.y;
+    jb.sh = v.y < 0;
+    jb.n0 = v.z;
+    jb.mt = v.w >> 8;
+    jb.nn = v.w & 255;
+    jb.np = (jb.nn + 15) & ~15;
+    jb.bsel = jb.np <= 16 ? 0 : jb.np <= 32 ? 1 : jb.np <= 64 ? 2 : 3;
+    return jb;
+  };
+  if (warp < 2) {  // two of the epilogue warps, before their first job
+    for (int i = tid; i < kJobCap; i += 64) {
+      int j = bid;
+      for (int r = 0; r < i && j < njobs; ++r) j = next_pos(j);
+      if (j < njobs) {
+        const Job jb = job_of(j);
+        s_job[i] = make_int4(jb.off, jb.slot, jb.n0, (jb.mt << 8) | jb.nn);
+      }
+    }
+  }
+  __syncthreads();
 
   if (warp == 12) {
     // ================= raw producer: codes and scales =================
     if (lane == 0) {
       int rcnt = 0;
-      for (int j = bid; j < njobs && !*abort_flag; j += G) {
-        const Job jb = job_of(j);
+      for (int j = bid, ji = 0; j < njobs && !*abort_flag; j = next_pos(j), ++ji) {
+        const Job jb = job_at(ji, j);
         const int K = k_of(jb);
         const int row0 = (jb.sh ? 0 : jb.slot * (GU ? a.I : a.H)) + jb.mt * job_rows<GU>();
         bool ok = true;
@@ -391,8 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     // lanes that are never read
     if (lane == 0) {
       int bcnt = 0;
-      for (int j = bid; j < njobs && !*abort_flag; j += G) {
-        const Job jb = job_of(j);
+      for (int j = bid, ji = 0; j < njobs && !*abort_flag; j = next_pos(j), ++ji) {
+        const Job jb = job_at(ji, j);
         const uint32_t bbytes = (16u << jb.bsel) * 128;  // one box
         const int spb = 8 >> jb.bsel;                      // boxes per slot
         bool ok = true;
@@ -421,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     const uint64_t xd0 = sdesc_sw128(sB);
     int acnt = 0, bcnt = 0, jcnt = 0;
     AccUse au{0, 0, 0};
-    for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
-      const Job jb = job_of(j);
+    for (int j = bid; j < njobs && !*abort_flag; j = next_pos(j), ++jcnt) {
+      const Job jb = job_at(jcnt, j);
       const int ab = GU ? 0 : jcnt & 1;
       int gb0 = 0, gb1 = 0;
       uint32_t gbase = 0, uoff = 128;
@@ -519,8 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     const uint32_t rsw = (uint32_t)(r & 7);
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + kTmA + m * kTmAMat;
     int rcnt = 0, acnt = 0;
-    for (int j = bid; j < njobs && !*abort_flag; j += G) {
-      const Job jb = job_of(j);
+    for (int j = bid, ji = 0; j < njobs && !*abort_flag; j = next_pos(j), ++ji) {
+      const Job jb = job_at(ji, j);
       const int K = k_of(jb);
       bool ok = true;
       for (int kr = 0; kr < K / 256 && ok; ++kr) {
@@ -579,8 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     // consecutive fp16 of one token's h row.
     const int row = qw * 32 + lane;
     AccUse au{0, 0, 0};
-    for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
-      const Job jb = job_of(j);
+    for (int j = bid; j < njobs && !*abort_flag; j = next_pos(j), ++jcnt) {
+      const Job jb = job_at(jcnt, j);
       int gb0, gb1;
       uint32_t gbase, uoff;
       au.next(jb.np, gb0, gb1, gbase, uoff);
@@ -638,8 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_kernel(const __grid_constant__
     // columns are the job's tokens; each warp store is a contiguous 128-byte
     // segment of one token's partial row.
     const int row = qw * 32 + lane;
-    for (int j = bid; j < njobs && !*abort_flag; j += G, ++jcnt) {
-      const Job jb = job_of(j);
+    for (int j = bid; j < njobs && !*abort_flag; j = next_pos(j), ++jcnt) {
+      const Job jb = job_at(jcnt, j);
       const int ab = jcnt & 1;
       // the routing weights of the job's pairs, fetched while its MMAs run
       float* colf = s_colf[ab];
