@@ -236,6 +236,58 @@ __global__ void __launch_bounds__(1024) permute_scatter_kernel(const int32_t* __
   }
 }
 
+// Steps 2 and 3 in one launch for up to kScanChunks chunks: every CTA derives
+// its chunk's bases (the counts of the chunks before it) and the expert
+// offsets from the histograms itself, then places its pairs; CTA 0 also
+// writes the offsets and the lists.
+constexpr int kScanChunks = 64;
+__global__ void __launch_bounds__(1024) permute_place_kernel(const int32_t* __restrict__ ids, int T, int E,
+                                                             int k, int n_chunks,
+                                                             const int32_t* __restrict__ slot_map, int S,
+                                                             int has_shared, PermuteOut o) {
+  __shared__ int s_cnt[kMaxE];
+  __shared__ int s_off[kMaxE + 1];
+  __shared__ int s_base[kMaxE];
+  __shared__ int s_warp[32];
+  __shared__ int s_total;
+  __shared__ __align__(16) uint8_t s_rc[kMaxE][32];
+  const int tid = threadIdx.x, c = blockIdx.x;
+  const int P = T * k;
+  const int p0 = c * kChunk;
+  const int n = min(kChunk, P - p0);
+  int e = 0;
+  if (tid < n) e = load_id(ids, p0 + tid, E, o.status);
+  int base = 0, tot = 0;
+  if (tid < E) {
+    for (int c0 = 0; c0 < n_chunks; c0 += 8) {  // 8 chunks' counts in flight at a time
+      int h[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) h[u] = c0 + u < n_chunks ? __ldcg(o.hist + (size_t)(c0 + u) * E + tid) : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        base += c0 + u < c ? h[u] : 0;
+        tot += h[u];
+      }
+    }
+    s_base[tid] = base;
+    s_cnt[tid] = tot;
+  }
+  const int rank = block_stable_rank(e, tid < n, s_rc);  // syncs the block
+  const int off = block_excl_scan(tid < E ? tot : 0, s_warp, &s_total);
+  if (tid < E) s_off[tid] = off;
+  if (tid == 0) s_off[E] = P;
+  __syncthreads();
+  if (tid < n) {
+    const int pos = s_off[e] + s_base[e] + rank;
+    o.sorted_pair[pos] = p0 + tid;
+    o.pair_pos[p0 + tid] = pos;
+  }
+  if (c != 0) return;
+  if (tid < E) o.offsets[tid] = s_off[tid];
+  if (tid == 0) o.offsets[E] = P;
+  build_lists(E, P, T, S, has_shared != 0, slot_map, s_cnt, s_off, s_warp, &s_total, o);
+}
+
 int cu_bound(int T, int E, int k, bool has_shared) {
   const int P = T * k;
   const int sh = has_shared ? (T + kTokTile - 1) / kTokTile : 0;
@@ -257,6 +309,12 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, const int32_
   launch_begin(K_PERMUTE, st);
   permute_hist_kernel<<<nc, 1024, 0, st>>>(ids, P, E, o);
   launch_end(st);
+  if (nc <= kScanChunks) {
+    launch_begin(K_PERMUTE, st);
+    permute_place_kernel<<<nc, 1024, 0, st>>>(ids, T, E, k, nc, slot_map, S, has_shared ? 1 : 0, o);
+    launch_end(st);
+    return cudaGetLastError();
+  }
   launch_begin(K_PERMUTE, st);
   permute_scan_kernel<<<1, 1024, 0, st>>>(T, E, k, nc, slot_map, S, has_shared ? 1 : 0, o);
   launch_end(st);
