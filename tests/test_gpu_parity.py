@@ -330,6 +330,46 @@ def test_prefill_sampled_rows():
     check_y(out["y"][rows], y, what="prefill sampled rows")
 
 
+def _scale_scales(s_bits, factor, mask=None):
+    """fp16 scale bit patterns times `factor` (rounded to fp16), where mask."""
+    h = s_bits.view(torch.float16).float()
+    scaled = (h * factor).to(torch.float16).float()
+    h = scaled if mask is None else torch.where(mask, scaled, h)
+    return h.to(torch.float16).view(torch.int16).contiguous()
+
+
+@pytest.mark.parametrize("case", ["down", "gateup", "subnormal", "mixed"])
+def test_prefill_small_scales(case):
+    """Prefill with small fp16 block scales: q * s must stay one rounding of the
+    exact product for every scale, down to subnormal ones (a form that takes
+    16 q times s / 16, say, would lose that below 2^-10). The scales of a whole
+    matrix kind are made small (x scaled up where needed, so that h stays a
+    normal fp16 number), or subnormal, or small in a random half of the blocks
+    of every matrix: y matches the oracle, which uses the same fp16 scales."""
+    cfg = synth.MoeConfig("pf_small_" + case, H=512, I=256, E=16, k=4, T=96, shared_I=256, zipf_s=1.0)
+    inp = synth.make_layer(cfg, 21)
+    g = torch.Generator().manual_seed(5)
+    kinds = {"down": ("down_s",), "gateup": ("gate_s", "up_s"), "subnormal": ("down_s",),
+             "mixed": ("gate_s", "up_s", "down_s")}[case]
+    factor = 2.0 ** -12 if case == "subnormal" else 2.0 ** -6
+    for name in kinds:
+        m = None
+        if case == "mixed":
+            m = torch.rand(getattr(inp, name).shape, generator=g) < 0.5
+        setattr(inp, name, _scale_scales(getattr(inp, name), factor, m))
+        ms = None if m is None else torch.rand(inp.sh[name].shape, generator=g) < 0.5
+        inp.sh[name] = _scale_scales(inp.sh[name], factor, ms)
+    if case == "gateup":  # x 64 times larger (exact in bf16) keeps g, u and h in range
+        xf = torch.from_numpy(synth.bf16_bits_to_f32(inp.x.numpy())) * 64.0
+        inp.x = synth.f32_to_bf16_bits(xf).contiguous()
+    for name in kinds:  # the three-shift form is exercised
+        assert (np.abs(getattr(inp, name).view(torch.float16).float().numpy()) < 2.0 ** -10).any()
+    out, _ = run_layer(inp)
+    ids, w, we, y = oracle_layer(inp, inp.logits.numpy())
+    assert np.array_equal(out["ids"], ids)
+    check_y(out["y"], y, what=f"small scales: {case}")
+
+
 @pytest.mark.parametrize("T", [1, 3, 5, 13, 16, 17, 33, 100])
 def test_ragged_windows(T):
     cfg = synth.MoeConfig("rag", H=512, I=256, E=32, k=4, T=T, shared_I=256, zipf_s=1.0)
