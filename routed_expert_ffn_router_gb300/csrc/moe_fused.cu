@@ -33,7 +33,8 @@
 //    units, which the CTAs that are running take from the queue;
 //  * once every unit is published, the CTAs share the reduction
 //    y = sum_j w_j sum_g p(e_j, g) + sum_g p(shared, g) in a fixed order, so y is
-//    deterministic; the last CTA to exit resets the cross-CTA counters.
+//    deterministic; once past the wait for the units, each CTA counts itself
+//    out, and the last one resets the cross-CTA counters.
 // Every expert a window touches (and the shared expert, Strata BATCHING,
 // "Several requests at once") is read from HBM exactly once.
 #include <cuda.h>
@@ -74,7 +75,9 @@ constexpr uint32_t kBf16NegMagic = 0xC308C308u;  // bf16 -136
 constexpr uint32_t kF16NegMagic = 0xE408E408u;   // f16 -1032
 
 // cross-CTA counters (int32 offsets in the workspace sync region)
-constexpr int kSyncDone = 0, kSyncUnits = 1, kSyncQueue = 2;
+// (the exit count has a cache line of its own: the units counter is still
+// polled, and the queue drawn, while CTAs count themselves out)
+constexpr int kSyncDone = 64, kSyncUnits = 1, kSyncQueue = 2;
 
 // Jobs of full units (kUI intermediate rows) and half units (64): gate/up
 // kind 2 s, down kind 2 s + 1 for unit size s = 0 (full), 1 (half).
@@ -725,7 +728,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
       }
     }
     __syncwarp();
-    named_bar_arrive(kBarReduce, kCW * 32 + 32);
+    // past this barrier the CTA's consumers no longer read the cross-CTA
+    // counters and its producer draws no more units: count the CTA out, off
+    // the reduction's path (the last CTA resets the counters for the next call)
+    named_bar_sync(kBarReduce, kCW * 32 + 32);
+    if (lane == 0 && atomicAdd(a.sync + kSyncDone, 1) == G - 1) {
+      a.sync[kSyncUnits] = 0;
+      a.sync[kSyncQueue] = 0;
+      a.sync[kSyncDone] = 0;
+    }
   } else {
     // ================= consumers =================
     const int cw = warp - 1, mw = cw & 3, kh = cw >> 2, ct = tid - 32;
@@ -1017,17 +1028,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     }
   }
 
-  // ---- the last CTA out resets the cross-CTA counters for the next call
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(a.sync + kSyncDone, 1) == G - 1) {
-      a.sync[kSyncUnits] = 0;
-      a.sync[kSyncQueue] = 0;
-      a.sync[kSyncDone] = 0;
-      __threadfence();
-    }
-  }
 }
 
 }  // namespace fused
