@@ -175,6 +175,60 @@ moe_status moe_layer_forward(const moe_layer_desc *L, const float *logits, const
                              int32_t *ids, float *w, int32_t *miss_ids, int32_t *n_miss,
                              void *ws, size_t ws_bytes, void *stream);
 
+/* ---- Several layers in one launch ----
+ * The whole decode pass of a stack of MoE layers as one persistent kernel
+ * (SGLang port post, section 3: the 48-layer pass captured as one graph; its
+ * grouped-kernel figures show the per-launch cost a pass of 48 layers pays).
+ * Each layer is moe_layer_forward on its own buffers: routing of its logits,
+ * permutation, the held experts' FFN and the shared expert, the ordered
+ * combine into its y (bitwise the same results as moe_layer_forward on that
+ * layer). Layer l + 1 starts only after every CTA has finished layer l (a
+ * grid-wide barrier), as a model whose next router input depends on this
+ * layer's output requires. All layers take the one-launch decode kernel: bf16
+ * x, 1 <= T <= 16, H a multiple of 512 up to 8192, I and shared_I multiples
+ * of 256 (else MOE_ERR_UNSUPPORTED). */
+
+/* One layer's DEVICE buffers, as moe_layer_forward takes them: logits [T][E]
+ * fp32, x [T][H] bf16 (16-byte aligned), slot_map [E] (nullable = every
+ * expert in slot e), y [T][H] fp32 (16-byte aligned), ids [T][k], w [T][k],
+ * miss_ids [E], n_miss [1]. */
+typedef struct {
+  const float *logits;
+  const void *x;
+  const int32_t *slot_map;
+  float *y;
+  int32_t *ids;
+  float *w;
+  int32_t *miss_ids;
+  int32_t *n_miss;
+} moe_layer_io;
+
+/* Bytes of a plan for n_layers layers (DEVICE memory the caller allocates,
+ * 64-byte aligned); 0 if n_layers is out of 1 .. 124. */
+size_t moe_decode_stack_plan_bytes(int32_t n_layers);
+
+/* Build the plan of n_layers layers (layers and io: HOST arrays [n_layers])
+ * for windows of T rows on workspace ws (at least moe_workspace_bytes of
+ * every layer for T; shared by all layers): the per-layer kernel arguments
+ * with their TMA descriptors, encoded on the host and copied into plan. It
+ * synchronises `stream`: call it once, outside the hot path and outside any
+ * stream capture. The plan holds the pointers given: it stays valid while
+ * those buffers, the weight pools and ws do. Errors as moe_layer_forward,
+ * plus MOE_ERR_INVALID for a plan smaller than moe_decode_stack_plan_bytes or
+ * not 64-byte aligned. */
+moe_status moe_decode_stack_prepare(const moe_layer_desc *layers, const moe_layer_io *io,
+                                    int32_t n_layers, int32_t T, void *plan, size_t plan_bytes,
+                                    void *ws, size_t ws_bytes, void *stream);
+
+/* Run the prepared stack: one cooperative launch on `stream` (one CTA per SM,
+ * all resident; MOE_ERR_CUDA if the device cannot hold them all). n_layers
+ * and T as prepared; ws the prepared workspace. Asynchronous and capturable
+ * once the plan exists. Device-detected problems go to ws's status word as for
+ * moe_layer_forward; a CTA that gives up (an expired bounded wait) ends the
+ * launch after its layer, and the later layers' outputs are left unwritten. */
+moe_status moe_decode_stack(const void *plan, int32_t n_layers, int32_t T, void *ws,
+                            size_t ws_bytes, void *stream);
+
 /* The routed-expert FFN for callers that cannot allocate device memory. The
  * Strata pages have no counterpart of this entry point: it exists for code
  * that cannot obtain a workspace (inside a framework whose allocator owns all

@@ -30,7 +30,8 @@ EXPORTS = ("moe_router_logits", "moe_route", "moe_permute", "moe_expert_ffn", "m
            "moe_cache_rebalance", "moe_cache_slot_map", "moe_cache_heat",
            "moe_cache_swapped_total", "moe_cache_profile_write", "moe_cache_profile_load",
            "moe_trace_write", "moe_trace_read", "moe_mailbox_create", "moe_mailbox_destroy",
-           "moe_mailbox_pairs", "moe_mailbox_compute", "moe_mailbox_inject", "moe_mailbox_add")
+           "moe_mailbox_pairs", "moe_mailbox_compute", "moe_mailbox_inject", "moe_mailbox_add",
+           "moe_decode_stack_plan_bytes", "moe_decode_stack_prepare", "moe_decode_stack")
 
 
 class MoeError(RuntimeError):
@@ -50,6 +51,12 @@ class moe_layer_desc(ctypes.Structure):
                 ("shared_I", ctypes.c_int32),
                 ("shared_gate", moe_qmat), ("shared_up", moe_qmat), ("shared_down", moe_qmat),
                 ("pick_counts", ctypes.c_void_p), ("pick_max_rows", ctypes.c_int32)]
+
+
+class moe_layer_io(ctypes.Structure):
+    _fields_ = [("logits", ctypes.c_void_p), ("x", ctypes.c_void_p), ("slot_map", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("ids", ctypes.c_void_p), ("w", ctypes.c_void_p),
+                ("miss_ids", ctypes.c_void_p), ("n_miss", ctypes.c_void_p)]
 
 
 class moe_cache_params(ctypes.Structure):
@@ -101,6 +108,10 @@ def load(path: str = LIB_PATH):
             "moe_profile_kind_name": ([ctypes.c_int32], ctypes.c_char_p),
             "moe_expert_ffn_static": ([D, P, i32, i32, P, P, P, P, P, P, P], i32),
             "moe_static_read_status": ([P, ctypes.POINTER(ctypes.c_int32)], i32),
+            "moe_decode_stack_plan_bytes": ([ctypes.c_int32], sz),
+            "moe_decode_stack_prepare": ([D, ctypes.POINTER(moe_layer_io), ctypes.c_int32,
+                                          ctypes.c_int32, P, sz, P, sz, P], i32),
+            "moe_decode_stack": ([P, ctypes.c_int32, ctypes.c_int32, P, sz, P], i32),
             "moe_cache_state_bytes": ([ctypes.POINTER(moe_cache_params), P], sz),
             "moe_cache_init": ([P, sz, ctypes.POINTER(moe_cache_params), P], i32),
             "moe_cache_set_resident": ([P, ctypes.c_int32, P, ctypes.c_int32], i32),
@@ -207,6 +218,25 @@ def moe_layer_forward(desc, logits, x, x_dtype, T, slot_map, y, ids, w, miss_ids
     _check("moe_layer_forward", load().moe_layer_forward(
         ctypes.byref(desc), _ptr(logits), _ptr(x), x_dtype, T, _ptr(slot_map), _ptr(y), _ptr(ids),
         _ptr(w), _ptr(miss_ids), _ptr(n_miss), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_decode_stack_plan_bytes(n_layers: int) -> int:
+    return int(load().moe_decode_stack_plan_bytes(n_layers))
+
+
+def moe_decode_stack_prepare(descs, ios, T, plan, plan_bytes, ws, ws_bytes, stream=None):
+    """descs: sequence of moe_layer_desc; ios: sequence of moe_layer_io (device pointers)."""
+    n = len(descs)
+    D = (moe_layer_desc * n)(*descs)
+    IO = (moe_layer_io * n)(*ios)
+    _check("moe_decode_stack_prepare",
+           load().moe_decode_stack_prepare(D, IO, n, T, _ptr(plan), plan_bytes, _ptr(ws), ws_bytes,
+                                           _stream(stream)))
+
+
+def moe_decode_stack(plan, n_layers, T, ws, ws_bytes, stream=None):
+    _check("moe_decode_stack",
+           load().moe_decode_stack(_ptr(plan), n_layers, T, _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def moe_workspace_bytes(desc, T) -> int:

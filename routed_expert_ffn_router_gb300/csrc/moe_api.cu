@@ -258,7 +258,8 @@ moe_status moe_profile_totals(int32_t kind, double* total_ms, int64_t* count) {
 
 const char* moe_profile_kind_name(int32_t kind) {
   static const char* names[K_NUM_KINDS] = {"router_logits", "route", "permute", "x_prep",
-                                           "gateup", "down", "combine", "fused_decode"};
+                                           "gateup", "down", "combine", "fused_decode",
+                                           "fused_stack"};
   if (kind < 0 || kind >= K_NUM_KINDS) return "";
   return names[kind];
 }
@@ -480,6 +481,70 @@ moe_status moe_layer_forward(const moe_layer_desc* L, const float* logits, const
   cudaError_t e = launch_route(logits, T, L->E, L->k, ids, w, at<int32_t>(ws, Lw.status), st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   return expert_ffn_impl(L, x, x_dtype, T, ids, w, slot_map, y, miss_ids, n_miss, ws, ws_bytes, st);
+}
+
+
+size_t moe_decode_stack_plan_bytes(int32_t n_layers) {
+  if (n_layers < 1 || n_layers > fused_stack_max_layers()) return 0;
+  return fused_stack_plan_bytes(n_layers);
+}
+
+moe_status moe_decode_stack_prepare(const moe_layer_desc* layers, const moe_layer_io* io,
+                                    int32_t n_layers, int32_t T, void* plan, size_t plan_bytes,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  if (!layers || !io || !plan) return MOE_ERR_INVALID;
+  if (n_layers < 1 || T < 1) return MOE_ERR_INVALID;
+  if (n_layers > fused_stack_max_layers()) return MOE_ERR_UNSUPPORTED;
+  if (plan_bytes < fused_stack_plan_bytes(n_layers) || (reinterpret_cast<uintptr_t>(plan) & 63u))
+    return MOE_ERR_INVALID;
+  std::vector<FusedLaunch> fl((size_t)n_layers);
+  for (int l = 0; l < n_layers; ++l) {
+    const moe_layer_desc* Ld = &layers[l];
+    const moe_layer_io& o = io[l];
+    moe_status s = check_desc(Ld);
+    if (s != MOE_OK) return s;
+    if (!pairs_ok(T, Ld->k)) return MOE_ERR_UNSUPPORTED;
+    if (!fused_decode_supported(Ld->H, Ld->I, Ld->shared_I, T, true)) return MOE_ERR_UNSUPPORTED;
+    const WsLayout Lw = ws_layout(Ld->E, Ld->k, T, Ld->H, Ld->I, Ld->shared_I);
+    if ((s = check_ws(ws, ws_bytes, Lw.total)) != MOE_OK) return s;
+    if (!o.logits || !o.x || !o.y || !o.ids || !o.w || !o.miss_ids || !o.n_miss) return MOE_ERR_INVALID;
+    if (!aligned16(o.x) || !aligned16(o.y)) return MOE_ERR_INVALID;
+    FusedLaunch& f = fl[(size_t)l];
+    f.gq = Ld->gate.q; f.gs = Ld->gate.scale;
+    f.uq = Ld->up.q;   f.us = Ld->up.scale;
+    f.dq = Ld->down.q; f.ds = Ld->down.scale;
+    if (Ld->shared_I > 0) {
+      f.sgq = Ld->shared_gate.q; f.sgs = Ld->shared_gate.scale;
+      f.suq = Ld->shared_up.q;   f.sus = Ld->shared_up.scale;
+      f.sdq = Ld->shared_down.q; f.sds = Ld->shared_down.scale;
+    }
+    f.H = Ld->H; f.I = Ld->I; f.shI = Ld->shared_I; f.E = Ld->E; f.k = Ld->k; f.S = Ld->S;
+    f.T = T; f.Imax = Lw.Imax; f.rows_cap = Lw.P + T;
+    f.logits = o.logits;
+    f.x = o.x; f.slot_map = o.slot_map;
+    f.ids_out = o.ids; f.w_out = o.w; f.y = o.y; f.miss_ids = o.miss_ids; f.n_miss = o.n_miss;
+    f.hhi = at<uint16_t>(ws, Lw.hhi);
+    f.hlo = at<uint16_t>(ws, Lw.hlo);
+    f.hcorr = at<float>(ws, Lw.hsum);
+    f.partial = at<float>(ws, Lw.partial);
+    f.status = at<int32_t>(ws, Lw.status);
+    f.sync = at<int32_t>(ws, Lw.sync);
+    f.picks = picks_of(Ld, T);
+  }
+  return cuda_status(fused_stack_prepare(fl.data(), n_layers, plan, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_decode_stack(const void* plan, int32_t n_layers, int32_t T, void* ws, size_t ws_bytes,
+                            void* stream) {
+  g_launches = 0;
+  if (!plan || n_layers < 1 || T < 1 || T > 16) return MOE_ERR_INVALID;
+  if (n_layers > fused_stack_max_layers()) return MOE_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < kWsHeadBytes || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_WORKSPACE;
+  const WsLayout Lw = ws_layout(1, 1, 1, 128, 128, 0);  // the head: status and counters
+  return cuda_status(launch_fused_stack(plan, n_layers, T, at<int32_t>(ws, Lw.sync),
+                                        at<int32_t>(ws, Lw.status), static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

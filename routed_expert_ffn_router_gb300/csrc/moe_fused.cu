@@ -468,9 +468,22 @@ struct Producer {
   }
 };
 
+// Ring state a CTA carries from one layer to the next when one launch runs
+// several layers: the producer's jobs issued, units taken and published; the
+// consumers' ring position and units consumed.
+struct RingState {
+  int pj, pui, ppd;
+  int cslot, cphase, ccs, cucnt;
+};
+
+// One layer's window (the whole work of decode_layer_kernel). `first`: the
+// launch's first layer (barrier set-up, programmatic dependent launch);
+// `count_out`: count the CTA out of the layer's cross-CTA counters after its
+// reduction wait (the last CTA resets them); a launch of several layers
+// resets them itself at its end.
 // MAXNT: n8 token tiles at most (1 for windows of up to 8 rows, 2 beyond).
 template <int MAXNT>
-__global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_constant__ Args a) {
+__device__ __forceinline__ bool layer_body(const Args& a, RingState& rs, bool first, bool count_out) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ int s_ids[kMaxT][kMaxK];
   __shared__ uint32_t s_tokmask[kMaxE];
@@ -508,14 +521,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
   volatile int* abort_flag = &s_abort;  // read in loops without barriers
 
   if (tid == 0) {
-    s_abort = 0;
-    for (int i = 0; i < a.nst; ++i) {
-      mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, kCW);
+    if (first) {
+      s_abort = 0;
+      for (int i = 0; i < a.nst; ++i) {
+        mbar_init(full0 + 8 * i, 1);
+        mbar_init(empty0 + 8 * i, kCW);
+      }
+      for (int i = 0; i < kPubBars; ++i) mbar_init(pub0 + 8 * i, kPubCount);
+      fence_barrier_init();
     }
-    for (int i = 0; i < kPubBars; ++i) mbar_init(pub0 + 8 * i, kPubCount);
-    fence_barrier_init();
-    // the tensor maps' descriptors (kernel parameters), fetched ahead of use
+    // the tensor maps' descriptors (kernel parameters or a plan in global
+    // memory), fetched ahead of use
     const CUtensorMap* maps[] = {&a.tm_gc, &a.tm_uc, &a.tm_dc, &a.tm_gs, &a.tm_us, &a.tm_ds, &a.tm_x,
                                  &a.tm_gch, &a.tm_uch, &a.tm_dch, &a.tm_gsh, &a.tm_ush};
     for (const CUtensorMap* m : maps) prefetch_tensormap(m);
@@ -526,12 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     }
     // the next kernel of the stream may be scheduled now: it takes an SM only
     // when a CTA of this one exits, and waits for this grid before reading
-    griddep_launch_dependents();
+    if (first) griddep_launch_dependents();
   }
   for (int e = tid; e < E; e += kThreads) s_tokmask[e] = 0;
   // nothing above reads global memory: from here on the previous kernel of the
   // stream (which may have written the inputs or this workspace) is complete
-  griddep_wait();
+  if (first) griddep_wait();
   // the slot map comes in by asynchronous copies while the routing runs
   for (int e = tid; e < E; e += kThreads) {
     if (a.slot_map) cp_async_4(&s_slot[e], a.slot_map + e);
@@ -662,8 +678,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     if (lane == 0) {
       // ================= producer (one thread) =================
       fence_proxy_async_shared();  // the top-k scratch in stage memory precedes the TMA writes
+      const int j0 = rs.pj;  // the layer's first job
       Producer P{a, sbase, full0, empty0, pub0, s_hdr, s_act_slot, D, a.nst, a.stage_bytes,
-                     l2_evict_first_policy(), 0, 0, 0, 0, 0};
+                     l2_evict_first_policy(), j0, rs.pui, rs.ppd, j0 % a.nst, (j0 / a.nst) & 1};
       bool ok = true;
       int next = ticket;
       while (ok && !*abort_flag && ticket < sc.total) {
@@ -681,9 +698,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
         next = atomicAdd(a.sync + kSyncQueue, 1);  // needed at the next unit only
         for (int ch = 0; ch < nch && ok; ++ch) {
           ok = P.issue(2 * u.z, u.x, u.y, ch);
-          // the kernel's first stage lands before the rest of the ring is
+          // the layer's first stage lands before the rest of the ring is
           // requested (all SMs ask at once; the consumers start one stage earlier)
-          if (ok && P.j == 1) ok = mbar_wait_bounded(full0, 0, a.status);
+          if (ok && P.j == j0 + 1)
+            ok = mbar_wait_bounded(full0 + 8 * (j0 % a.nst), (j0 / a.nst) & 1, a.status);
         }
         for (int ch = 0; ch < nchd && ok; ++ch) ok = P.issue(2 * u.z + 1, u.x, u.y, ch);
         ticket = next;
@@ -702,6 +720,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
       // no copy may still be in flight when the CTA exits (bounded)
       for (int jj = P.j - 1; jj >= 0 && jj >= P.j - a.nst; --jj)
         mbar_wait_bounded(full0 + 8 * (jj % a.nst), (jj / a.nst) & 1, a.status);
+      rs.pj = P.j;
+      rs.pui = P.ui;
+      rs.ppd = P.pd;
     }
     __syncwarp();
   } else if (warp == kHelperWarp) {
@@ -732,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     // counters and its producer draws no more units: count the CTA out, off
     // the reduction's path (the last CTA resets the counters for the next call)
     named_bar_sync(kBarReduce, kCW * 32 + 32);
-    if (lane == 0 && atomicAdd(a.sync + kSyncDone, 1) == G - 1) {
+    if (count_out && lane == 0 && atomicAdd(a.sync + kSyncDone, 1) == G - 1) {
       a.sync[kSyncUnits] = 0;
       a.sync[kSyncQueue] = 0;
       a.sync[kSyncDone] = 0;
@@ -766,9 +787,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     float accd[kDnM][2][4];
     int browx[2] = {0, 0};  // x box row (token) of token slot nt*8 + g
     int browh[2] = {0, 0};  // h buffer row (slot) of token slot nt*8 + g
-    int cnt = 0, ntiles = 1, ucnt = 0;
+    int cnt = 0, ntiles = 1, ucnt = rs.cucnt;
     const int nst = a.nst;
-    int slot = 0, phase = 0, cslot = -1;  // ring position of the job being consumed
+    int slot = rs.cslot, phase = rs.cphase, cslot = rs.ccs;  // ring position of the job being consumed
     for (;;) {
       if (cslot >= 0 && ++slot == nst) {  // advance past the previous job
         slot = 0;
@@ -782,6 +803,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
       }
       const int4 hd = s_hdr[slot];
       if (hd.x == J_END) {
+        // the stage is released too, for a launch whose next layer reuses it
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * slot);
         publish();
         break;
       }
@@ -946,6 +970,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
     }
 
     if (bulk_wr) bulk_wait_all();
+    rs.cslot = slot;
+    rs.cphase = phase;
+    rs.ccs = cslot;
+    rs.cucnt = ucnt;
 
     // ---- reduction, once every unit of the window is published. Lane q of an
     // 8-lane group sums, for one output float4,
@@ -1027,7 +1055,68 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
       }
     }
   }
+  // a launch of several layers learns here whether this CTA gave up
+  if (count_out) return false;
+  __syncthreads();
+  return *abort_flag != 0;
+}
 
+// One window (T <= 16 rows) of one layer per launch.
+template <int MAXNT>
+__global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_constant__ Args a) {
+  RingState rs = {0, 0, 0, 0, 0, -1, 0};
+  layer_body<MAXNT>(a, rs, true, true);
+}
+
+// Several layers in one launch, one window each (the whole decode pass in one
+// call, as the SGLang port post's section 3 captures it in one graph): layer l
+// is layer_body on plan[l] (the arguments in global memory, tensor maps
+// 64-byte aligned; its cross-CTA counters at plan[l].sync), then a grid-wide
+// barrier, so that no CTA starts layer l + 1's routing before every CTA has
+// finished layer l (its output written, its partials read). The CTAs keep
+// their barrier ring, shared memory and descriptors from layer to layer. One
+// CTA per SM, all resident (a cooperative launch); every wait is bounded: a
+// CTA that gave up, or a barrier that timed out, ends the launch after the
+// layer (the status word says which).
+constexpr int kStackBar = 96, kStackAbort = 97, kStackDone = 98;
+constexpr int kStackBase = 128, kStackStride = 32;  // layer l's counters: sync + base + stride l
+
+template <int MAXNT>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_stack_kernel(const Args* __restrict__ plan, int L, int32_t* __restrict__ sync,
+                    int32_t* __restrict__ status) {
+  __shared__ int s_stop;
+  RingState rs = {0, 0, 0, 0, 0, -1, 0};
+  const int G = gridDim.x;
+  for (int l = 0; l < L; ++l) {
+    const bool aborted = layer_body<MAXNT>(plan[l], rs, l == 0, false);
+    if (threadIdx.x == 0) {
+      // the next layer's descriptors, fetched while the barrier completes
+      if (l + 1 < L) {
+        const Args& n = plan[l + 1];
+        const CUtensorMap* maps[] = {&n.tm_gc, &n.tm_uc, &n.tm_dc, &n.tm_gs, &n.tm_us, &n.tm_ds, &n.tm_x,
+                                     &n.tm_gch, &n.tm_uch, &n.tm_dch, &n.tm_gsh, &n.tm_ush};
+        for (const CUtensorMap* m : maps) prefetch_tensormap(m);
+      }
+      if (aborted) atomicOr(sync + kStackAbort, 1);
+      red_release_gpu_add(sync + kStackBar, 1);
+      int stop = wait_counter_bounded(sync + kStackBar, (l + 1) * G, status) ? 0 : 1;
+      if (ld_acquire_gpu(sync + kStackAbort)) stop = 1;
+      s_stop = stop;
+    }
+    __syncthreads();
+    if (s_stop) break;
+  }
+  // count out; the last CTA resets every counter the launch used
+  if (threadIdx.x == 0 && atomicAdd(sync + kStackDone, 1) == G - 1) {
+    for (int l = 0; l < L; ++l) {
+      sync[kStackBase + kStackStride * l + kSyncUnits] = 0;
+      sync[kStackBase + kStackStride * l + kSyncQueue] = 0;
+    }
+    sync[kStackBar] = 0;
+    sync[kStackAbort] = 0;
+    sync[kStackDone] = 0;
+  }
 }
 
 }  // namespace fused
@@ -1164,7 +1253,8 @@ int fused_partial_slices(int E, int k, int T, int I, int shI) {
   return (I > shI ? I : shI) / 64;
 }
 
-template <int NTX>
+// STACK: the kernel of several layers per launch (else one layer per launch).
+template <int NTX, bool STACK = false>
 static cudaError_t kernel_attrs(size_t* static_smem, int* optin) {
   static std::mutex mu;
   static size_t st = 0;
@@ -1172,7 +1262,8 @@ static cudaError_t kernel_attrs(size_t* static_smem, int* optin) {
   std::lock_guard<std::mutex> lk(mu);
   if (opt == 0) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, fused::decode_layer_kernel<NTX>);
+    cudaError_t e = STACK ? cudaFuncGetAttributes(&fa, fused::decode_stack_kernel<NTX>)
+                          : cudaFuncGetAttributes(&fa, fused::decode_layer_kernel<NTX>);
     if (e != cudaSuccess) return e;
     int dev = 0, o = 0;
     e = cudaGetDevice(&dev);
@@ -1187,12 +1278,12 @@ static cudaError_t kernel_attrs(size_t* static_smem, int* optin) {
 }
 
 // Stages that fit next to the kernel's static shared memory (0: not even two).
-template <int NTX>
+template <int NTX, bool STACK = false>
 static int stages_for(int TB) {
   constexpr int MT = fused::kMT;
   size_t st = 0;
   int optin = 0;
-  if (kernel_attrs<NTX>(&st, &optin) != cudaSuccess) {
+  if (kernel_attrs<NTX, STACK>(&st, &optin) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1259,10 +1350,10 @@ static cudaError_t launch_nt(fused::Args& a, cudaStream_t st) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st) {
+// The kernel arguments of one layer's window (tensor maps encoded on the host).
+static bool build_args(const FusedLaunch& f, fused::Args& a) {
   const int TB = box_rows(f.T);
   const int UI = fused::kUI, HI = fused::kUI / 2, DR = 256;  // down boxes of 256 rows
-  fused::Args a;
   std::memset(&a, 0, sizeof a);
   a.H = f.H; a.I = f.I; a.shI = f.shI; a.E = f.E; a.k = f.k; a.S = f.S; a.T = f.T;
   a.Gh = fused_partial_slices(f.E, f.k, f.T, f.I, f.shI);
@@ -1293,7 +1384,7 @@ cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st) {
          codes_map(&a.tm_sdch, f.sdq, f.shI, H, HI / 2, DR) &&
          scales_map(&a.tm_sgsh, f.sgs, H, f.shI, HI) &&
          scales_map(&a.tm_sush, f.sus, H, f.shI, HI);
-  if (!ok) return cudaErrorInvalidValue;
+  if (!ok) return false;
   a.logits = f.logits; a.ids_in = f.ids_in; a.w_in = f.w_in;
   a.slot_map = f.slot_map;
   a.ids_out = f.ids_out; a.w_out = f.w_out; a.y = f.y;
@@ -1301,7 +1392,95 @@ cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st) {
   a.partial = f.partial;
   a.status = f.status; a.sync = f.sync;
   a.picks = f.picks;
-  return TB == 8 ? launch_nt<1>(a, st) : launch_nt<2>(a, st);
+  return true;
+}
+
+cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st) {
+  fused::Args a;
+  if (!build_args(f, a)) return cudaErrorInvalidValue;
+  return a.TB == 8 ? launch_nt<1>(a, st) : launch_nt<2>(a, st);
+}
+
+// ---- several layers per launch
+size_t fused_stack_plan_bytes(int L) { return L > 0 ? (size_t)L * sizeof(fused::Args) : 0; }
+int fused_stack_max_layers() {
+  return (kSyncInts - fused::kStackBase) / fused::kStackStride;
+}
+
+cudaError_t fused_stack_prepare(const FusedLaunch* layers, int L, void* plan, cudaStream_t st) {
+  if (L < 1 || L > fused_stack_max_layers() || !plan) return cudaErrorInvalidValue;
+  const int TB = box_rows(layers[0].T);
+  const int nst = TB == 8 ? stages_for<1, true>(TB) : stages_for<2, true>(TB);
+  if (nst < 2) return cudaErrorInvalidValue;
+  std::vector<fused::Args> h((size_t)L);
+  for (int l = 0; l < L; ++l) {
+    fused::Args& a = h[(size_t)l];
+    std::memset(&a, 0, sizeof a);
+    FusedLaunch f = layers[l];
+    f.sync = layers[0].sync + fused::kStackBase + fused::kStackStride * l;
+    if (f.T != layers[0].T || !build_args(f, a)) return cudaErrorInvalidValue;
+    a.stage_bytes = fused::stage_bytes_for(fused::kMT, a.TB);
+    a.nst = nst;
+  }
+  cudaError_t e = cudaMemcpyAsync(plan, h.data(), h.size() * sizeof(fused::Args),
+                                  cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);  // the host copy goes out of scope
+  return e;
+}
+
+template <int NTX>
+static cudaError_t launch_stack_nt(const fused::Args* plan, int L, int TB, int nst, int32_t* sync,
+                                   int32_t* status, cudaStream_t st) {
+  constexpr int MT = fused::kMT;
+  const size_t smem = fused::smem_bytes(MT, NTX, nst, fused::stage_bytes_for(MT, TB), TB);
+  static std::mutex mu;
+  static size_t configured[64] = {};
+  {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+      cudaGetLastError();
+      return e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (smem > configured[dev]) {
+      e = cudaFuncSetAttribute(fused::decode_stack_kernel<NTX>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e;
+      }
+      configured[dev] = smem;
+    }
+  }
+  // every CTA waits for every other at each layer's barrier: a cooperative
+  // launch, which fails at launch instead of waiting when they cannot all be resident
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms());
+  cfg.blockDim = dim3(fused::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  launch_begin(K_FUSED_STACK, st);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, fused::decode_stack_kernel<NTX>, plan, L, sync, status);
+  launch_end(st);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_fused_stack(const void* plan, int L, int T, int32_t* sync, int32_t* status,
+                               cudaStream_t st) {
+  if (L < 1 || L > fused_stack_max_layers() || !plan || T < 1 || T > fused::kMaxT)
+    return cudaErrorInvalidValue;
+  const int TB = box_rows(T);
+  const int nst = TB == 8 ? stages_for<1, true>(TB) : stages_for<2, true>(TB);
+  if (nst < 2) return cudaErrorInvalidValue;
+  const fused::Args* p = static_cast<const fused::Args*>(plan);
+  return TB == 8 ? launch_stack_nt<1>(p, L, TB, nst, sync, status, st)
+                 : launch_stack_nt<2>(p, L, TB, nst, sync, status, st);
 }
 
 }  // namespace moe

@@ -12,6 +12,7 @@ namespace moe {
 // Kernel kinds for the optional event timing (moe_profile_*).
 enum KernelKind : int {
   K_ROUTER_LOGITS = 0, K_ROUTE, K_PERMUTE, K_X_PREP, K_GATEUP, K_DOWN, K_COMBINE, K_FUSED,
+  K_FUSED_STACK,
   K_NUM_KINDS
 };
 
@@ -115,5 +116,14 @@ bool fused_decode_supported(int H, int I, int shI, int T, bool x_bf16);
 // rows x slices x H floats).
 int fused_partial_slices(int E, int k, int T, int I, int shI);
 cudaError_t launch_fused_decode(const FusedLaunch& f, cudaStream_t st);
+// Several layers' windows in one launch: a plan of per-layer kernel arguments
+// in device memory (fused_stack_plan_bytes(L) bytes, 64-byte aligned), built
+// from the layers' launches (same T; the cross-CTA counters of layer l at
+// layers[0].sync + a per-layer offset) and copied there synchronously.
+size_t fused_stack_plan_bytes(int L);
+int fused_stack_max_layers();
+cudaError_t fused_stack_prepare(const FusedLaunch* layers, int L, void* plan, cudaStream_t st);
+cudaError_t launch_fused_stack(const void* plan, int L, int T, int32_t* sync, int32_t* status,
+                               cudaStream_t st);
 
 }  // namespace moe

@@ -85,3 +85,60 @@ class MoeLayer:
 
     def clear_status(self, stream=None):
         _lib.moe_workspace_init(self.ws_ptr, self.ws_bytes, stream)
+
+
+class DecodeStack:
+    """Several layers' decode windows in one launch (moe_decode_stack): one
+    workspace shared by the layers, a device plan of their kernel arguments
+    and each layer's output buffers. Marshalling only."""
+
+    def __init__(self, layers, logits, xs, T: int, slot_maps=None, device="cuda"):
+        """layers: sequence of synth.LayerInputs (device pools); logits[l] [T][E]
+        fp32 and xs[l] [T][H] bf16 device tensors, kept referenced here."""
+        self.device = torch.device(device)
+        self.T = T
+        self.L = len(layers)
+        self.inps = list(layers)
+        self.descs = [make_desc(inp) for inp in layers]
+        self.logits = list(logits)
+        self.xs = list(xs)
+        # each layer's slot map (its LayerInputs' own unless given; None = all held)
+        self.slot_maps = ([inp.slot_map for inp in layers] if slot_maps is None
+                          else list(slot_maps))
+        self.ws_bytes = max(_lib.moe_workspace_bytes(d, T) for d in self.descs)
+        if self.ws_bytes == 0:
+            raise ValueError("invalid layer description")
+        self.ws = torch.empty(self.ws_bytes + 256, dtype=torch.uint8, device=self.device)
+        self.ws_ptr = self.ws.data_ptr() + (-self.ws.data_ptr()) % 256
+        _lib.moe_workspace_init(self.ws_ptr, self.ws_bytes)
+        self.outs = []
+        for inp in layers:
+            cfg = inp.cfg
+            self.outs.append(dict(
+                y=torch.empty(T, cfg.H, dtype=torch.float32, device=self.device),
+                ids=torch.empty(T, cfg.k, dtype=torch.int32, device=self.device),
+                w=torch.empty(T, cfg.k, dtype=torch.float32, device=self.device),
+                miss_ids=torch.empty(cfg.E, dtype=torch.int32, device=self.device),
+                n_miss=torch.zeros(1, dtype=torch.int32, device=self.device)))
+        ios = []
+        for l in range(self.L):
+            o = self.outs[l]
+            sm = self.slot_maps[l]
+            ios.append(_lib.moe_layer_io(self.logits[l].data_ptr(), self.xs[l].data_ptr(),
+                                         None if sm is None else sm.data_ptr(), o["y"].data_ptr(),
+                                         o["ids"].data_ptr(), o["w"].data_ptr(),
+                                         o["miss_ids"].data_ptr(), o["n_miss"].data_ptr()))
+        self.plan_bytes = _lib.moe_decode_stack_plan_bytes(self.L)
+        if self.plan_bytes == 0:
+            raise ValueError("unsupported number of layers")
+        self.plan = torch.empty(self.plan_bytes + 64, dtype=torch.uint8, device=self.device)
+        self.plan_ptr = self.plan.data_ptr() + (-self.plan.data_ptr()) % 64
+        _lib.moe_decode_stack_prepare(self.descs, ios, T, self.plan_ptr, self.plan_bytes,
+                                      self.ws_ptr, self.ws_bytes)
+
+    def forward(self, stream=None):
+        _lib.moe_decode_stack(self.plan_ptr, self.L, self.T, self.ws_ptr, self.ws_bytes, stream)
+        return self.outs
+
+    def status(self, stream=None):
+        return _lib.moe_read_status(self.ws_ptr, stream)

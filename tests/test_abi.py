@@ -187,3 +187,29 @@ def test_pair_and_logit_counts_beyond_int32_are_refused(lib):
                                      4096, None) == _lib.MOE_ERR_UNSUPPORTED
     assert lib.moe_router_logits(4096, 0, 4096, 1 << 22, 128, 1024, 4096,
                                  None) == _lib.MOE_ERR_UNSUPPORTED
+
+
+def test_decode_stack_host_checks(lib):
+    # the plan size covers 1 .. 124 layers (the cross-CTA counters of each
+    # layer have a cache line of their own in the workspace head)
+    assert lib.moe_decode_stack_plan_bytes(0) == 0
+    assert lib.moe_decode_stack_plan_bytes(125) == 0
+    one = lib.moe_decode_stack_plan_bytes(1)
+    assert one > 0 and one % 64 == 0
+    assert lib.moe_decode_stack_plan_bytes(48) == 48 * one
+    d = (_lib.moe_layer_desc * 2)(_desc(), _desc())
+    io = (_lib.moe_layer_io * 2)(_lib.moe_layer_io(*([4096] * 8)), _lib.moe_layer_io(*([4096] * 8)))
+    ws = 1 << 20
+    # argument errors return before anything touches the device
+    assert lib.moe_decode_stack_prepare(None, io, 2, 4, 4096, one * 2, ws, 1 << 20, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_decode_stack_prepare(d, None, 2, 4, 4096, one * 2, ws, 1 << 20, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_decode_stack_prepare(d, io, 0, 4, 4096, one * 2, ws, 1 << 20, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_decode_stack_prepare(d, io, 2, 0, 4096, one * 2, ws, 1 << 20, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_decode_stack_prepare(d, io, 125, 4, 4096, one * 125, ws, 1 << 20, None) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_decode_stack_prepare(d, io, 2, 4, 4096, one, ws, 1 << 20, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_decode_stack_prepare(d, io, 2, 4, 4096 + 32, one * 2, ws, 1 << 20, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_decode_stack(None, 2, 4, ws, 1 << 20, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_decode_stack(4096, 2, 17, ws, 1 << 20, None) == _lib.MOE_ERR_INVALID
+    assert lib.moe_decode_stack(4096, 125, 4, ws, 1 << 20, None) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_decode_stack(4096, 2, 4, ws + 8, 1 << 20, None) == _lib.MOE_ERR_WORKSPACE
+    assert lib.moe_decode_stack(4096, 2, 4, ws, 1024, None) == _lib.MOE_ERR_WORKSPACE
