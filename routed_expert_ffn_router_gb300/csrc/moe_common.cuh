@@ -547,12 +547,13 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   return v;
 }
 
-// Spin until *p >= target (acquire), giving up after about a second with DEV_TIMEOUT.
+// Spin until *p >= target (acquire), giving up after about a second with
+// DEV_TIMEOUT. Each poll is one load's round trip (the thread waits for its
+// value), so the loop needs no sleep: one thread per CTA polls.
 __device__ __forceinline__ bool wait_counter_bounded(const int* p, int target, int32_t* status) {
   if (ld_acquire_gpu(p) >= target) return true;
   const long long t0 = cycles_now();
   for (uint32_t it = 1;; ++it) {
-    __nanosleep(64);
     if (ld_acquire_gpu(p) >= target) return true;
     if ((it & 15) == 0 && cycles_now() - t0 > kWaitCycles) {
       if (status) atomicOr(status, DEV_TIMEOUT);

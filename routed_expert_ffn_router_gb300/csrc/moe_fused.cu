@@ -970,10 +970,6 @@ __device__ __forceinline__ bool layer_body(const Args& a, RingState& rs, bool fi
     }
 
     if (bulk_wr) bulk_wait_all();
-    rs.cslot = slot;
-    rs.cphase = phase;
-    rs.ccs = cslot;
-    rs.cucnt = ucnt;
 
     // ---- reduction, once every unit of the window is published. Lane q of an
     // 8-lane group sums, for one output float4,
@@ -992,6 +988,14 @@ __device__ __forceinline__ bool layer_body(const Args& a, RingState& rs, bool fi
       s_reduce = go ? 1 : 0;
     }
     named_bar_sync(kBarReduce, kCW * 32 + 32);
+    // every consumer thread holds the same ring position; all of them have
+    // read the layer's start position before this barrier
+    if (ct == 0) {
+      rs.cslot = slot;
+      rs.cphase = phase;
+      rs.ccs = cslot;
+      rs.cucnt = ucnt;
+    }
     {
       if (s_reduce) {
         const int q = ct & 7, H4 = H / 4, NO = T * H4;
@@ -1086,7 +1090,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 decode_stack_kernel(const Args* __restrict__ plan, int L, int32_t* __restrict__ sync,
                     int32_t* __restrict__ status) {
   __shared__ int s_stop;
-  RingState rs = {0, 0, 0, 0, 0, -1, 0};
+  // the ring state lives in shared memory between layers (each role reads it
+  // at a layer's start and its owner writes it back at the end), so that no
+  // register is held across the layers
+  __shared__ RingState s_rs;
+  if (threadIdx.x == 0) s_rs = RingState{0, 0, 0, 0, 0, -1, 0};
+  __syncthreads();
+  RingState& rs = s_rs;
   const int G = gridDim.x;
   for (int l = 0; l < L; ++l) {
     const bool aborted = layer_body<MAXNT>(plan[l], rs, l == 0, false);
