@@ -220,6 +220,22 @@ moe_status moe_decode_stack_prepare(const moe_layer_desc *layers, const moe_laye
                                     int32_t n_layers, int32_t T, void *plan, size_t plan_bytes,
                                     void *ws, size_t ws_bytes, void *stream);
 
+/* The same for a chained stack with the router in the launch (the whole
+ * decode pass: the SGLang port post's section 3 runs the 48 layers, router
+ * included, in one captured graph). router_w: HOST array [n_layers] of DEVICE
+ * pointers to each layer's router weights [E][H] bf16 (16-byte aligned).
+ * Layer l computes logits[t][e] = sum_h x_l[t][h] * W_r[e][h] (bf16 products,
+ * fp32 sums in a fixed order: deterministic, within fp32 rounding of the
+ * exact value) into io[l].logits, which is then an OUTPUT, routes them, and
+ * runs the layer as above; its output also gives the next layer's input
+ * x_{l+1}[t][h] = bf16_rne(x_l[t][h] + y_l[t][h]) (the residual add, one fp32
+ * sum), written into io[l + 1].x. io[0].x is the caller's input; io[l].x for
+ * l >= 1 are written by the launch. All layers take the same H. */
+moe_status moe_decode_stack_prepare_routed(const moe_layer_desc *layers, const moe_layer_io *io,
+                                           const uint16_t *const *router_w, int32_t n_layers,
+                                           int32_t T, void *plan, size_t plan_bytes, void *ws,
+                                           size_t ws_bytes, void *stream);
+
 /* Run the prepared stack: one cooperative launch on `stream` (one CTA per SM,
  * all resident; MOE_ERR_CUDA if the device cannot hold them all). n_layers
  * and T as prepared; ws the prepared workspace. Asynchronous and capturable

@@ -31,7 +31,8 @@ EXPORTS = ("moe_router_logits", "moe_route", "moe_permute", "moe_expert_ffn", "m
            "moe_cache_swapped_total", "moe_cache_profile_write", "moe_cache_profile_load",
            "moe_trace_write", "moe_trace_read", "moe_mailbox_create", "moe_mailbox_destroy",
            "moe_mailbox_pairs", "moe_mailbox_compute", "moe_mailbox_inject", "moe_mailbox_add",
-           "moe_decode_stack_plan_bytes", "moe_decode_stack_prepare", "moe_decode_stack")
+           "moe_decode_stack_plan_bytes", "moe_decode_stack_prepare",
+           "moe_decode_stack_prepare_routed", "moe_decode_stack")
 
 
 class MoeError(RuntimeError):
@@ -111,6 +112,8 @@ def load(path: str = LIB_PATH):
             "moe_decode_stack_plan_bytes": ([ctypes.c_int32], sz),
             "moe_decode_stack_prepare": ([D, ctypes.POINTER(moe_layer_io), ctypes.c_int32,
                                           ctypes.c_int32, P, sz, P, sz, P], i32),
+            "moe_decode_stack_prepare_routed": ([D, ctypes.POINTER(moe_layer_io), P, ctypes.c_int32,
+                                                 ctypes.c_int32, P, sz, P, sz, P], i32),
             "moe_decode_stack": ([P, ctypes.c_int32, ctypes.c_int32, P, sz, P], i32),
             "moe_cache_state_bytes": ([ctypes.POINTER(moe_cache_params), P], sz),
             "moe_cache_init": ([P, sz, ctypes.POINTER(moe_cache_params), P], i32),
@@ -232,6 +235,18 @@ def moe_decode_stack_prepare(descs, ios, T, plan, plan_bytes, ws, ws_bytes, stre
     _check("moe_decode_stack_prepare",
            load().moe_decode_stack_prepare(D, IO, n, T, _ptr(plan), plan_bytes, _ptr(ws), ws_bytes,
                                            _stream(stream)))
+
+
+def moe_decode_stack_prepare_routed(descs, ios, router_w, T, plan, plan_bytes, ws, ws_bytes,
+                                    stream=None):
+    """router_w: sequence of device tensors (or pointers), one [E][H] bf16 per layer."""
+    n = len(descs)
+    D = (moe_layer_desc * n)(*descs)
+    IO = (moe_layer_io * n)(*ios)
+    W = (ctypes.c_void_p * n)(*[_ptr(w) for w in router_w])
+    _check("moe_decode_stack_prepare_routed",
+           load().moe_decode_stack_prepare_routed(D, IO, W, n, T, _ptr(plan), plan_bytes, _ptr(ws),
+                                                  ws_bytes, _stream(stream)))
 
 
 def moe_decode_stack(plan, n_layers, T, ws, ws_bytes, stream=None):

@@ -489,9 +489,10 @@ size_t moe_decode_stack_plan_bytes(int32_t n_layers) {
   return fused_stack_plan_bytes(n_layers);
 }
 
-moe_status moe_decode_stack_prepare(const moe_layer_desc* layers, const moe_layer_io* io,
-                                    int32_t n_layers, int32_t T, void* plan, size_t plan_bytes,
-                                    void* ws, size_t ws_bytes, void* stream) {
+static moe_status stack_prepare(const moe_layer_desc* layers, const moe_layer_io* io,
+                                const uint16_t* const* router_w, int32_t n_layers, int32_t T,
+                                void* plan, size_t plan_bytes, void* ws, size_t ws_bytes,
+                                void* stream) {
   g_launches = 0;
   if (!layers || !io || !plan) return MOE_ERR_INVALID;
   if (n_layers < 1 || T < 1) return MOE_ERR_INVALID;
@@ -510,6 +511,11 @@ moe_status moe_decode_stack_prepare(const moe_layer_desc* layers, const moe_laye
     if ((s = check_ws(ws, ws_bytes, Lw.total)) != MOE_OK) return s;
     if (!o.logits || !o.x || !o.y || !o.ids || !o.w || !o.miss_ids || !o.n_miss) return MOE_ERR_INVALID;
     if (!aligned16(o.x) || !aligned16(o.y)) return MOE_ERR_INVALID;
+    if (router_w) {
+      // chained: every layer the same H; layer l + 1's x is written by layer l
+      if (!router_w[l] || !aligned16(router_w[l]) || Ld->H != layers[0].H) return MOE_ERR_INVALID;
+      if (l + 1 < n_layers && !io[l + 1].x) return MOE_ERR_INVALID;
+    }
     FusedLaunch& f = fl[(size_t)l];
     f.gq = Ld->gate.q; f.gs = Ld->gate.scale;
     f.uq = Ld->up.q;   f.us = Ld->up.scale;
@@ -531,8 +537,26 @@ moe_status moe_decode_stack_prepare(const moe_layer_desc* layers, const moe_laye
     f.status = at<int32_t>(ws, Lw.status);
     f.sync = at<int32_t>(ws, Lw.sync);
     f.picks = picks_of(Ld, T);
+    if (router_w) {
+      f.router_w = router_w[l];
+      f.x_next = l + 1 < n_layers ? static_cast<uint16_t*>(const_cast<void*>(io[l + 1].x)) : nullptr;
+    }
   }
   return cuda_status(fused_stack_prepare(fl.data(), n_layers, plan, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_decode_stack_prepare(const moe_layer_desc* layers, const moe_layer_io* io,
+                                    int32_t n_layers, int32_t T, void* plan, size_t plan_bytes,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  return stack_prepare(layers, io, nullptr, n_layers, T, plan, plan_bytes, ws, ws_bytes, stream);
+}
+
+moe_status moe_decode_stack_prepare_routed(const moe_layer_desc* layers, const moe_layer_io* io,
+                                           const uint16_t* const* router_w, int32_t n_layers,
+                                           int32_t T, void* plan, size_t plan_bytes, void* ws,
+                                           size_t ws_bytes, void* stream) {
+  if (!router_w) return MOE_ERR_INVALID;
+  return stack_prepare(layers, io, router_w, n_layers, T, plan, plan_bytes, ws, ws_bytes, stream);
 }
 
 moe_status moe_decode_stack(const void* plan, int32_t n_layers, int32_t T, void* ws, size_t ws_bytes,

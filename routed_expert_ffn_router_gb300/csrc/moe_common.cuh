@@ -562,6 +562,25 @@ __device__ __forceinline__ bool wait_counter_bounded(const int* p, int target, i
   }
 }
 
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// The same wait without acquire ordering (for counters that order nothing
+// but their own value).
+__device__ __forceinline__ bool wait_counter_relaxed(const int* p, int target, int32_t* status) {
+  if (ld_relaxed_gpu(p) >= target) return true;
+  const long long t0 = cycles_now();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_relaxed_gpu(p) >= target) return true;
+    if ((it & 15) == 0 && cycles_now() - t0 > kWaitCycles) {
+      if (status) atomicOr(status, DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Release-ordered atomic add at GPU scope: this thread's earlier writes, and
 // those it observed through a CTA barrier, are visible before the add.
 __device__ __forceinline__ void red_release_gpu_add(int* p, int v) {

@@ -115,6 +115,12 @@ struct Args {
   int32_t* status;
   int32_t* sync;
   int32_t* picks;  // nullable: one pick per distinct expert of the window
+  // a stack of chained layers with the router in the launch (else null):
+  // logits = x W_r^T from router_w [E][H] bf16 into `logits` (which the
+  // routing then reads), and x_next [T][H] bf16 = bf16(x + y) for the next layer
+  const uint16_t* router_w;
+  const uint16_t* xg;  // x [T][H] bf16 for the router and the residual add
+  uint16_t* x_next;
 };
 
 // Stage layouts (byte offsets from the 1024-aligned stage base), UI = 32 MT
@@ -1054,6 +1060,17 @@ __device__ __forceinline__ bool layer_body(const Args& a, RingState& rs, bool fi
           if (live && q == 0) {
             float* yp = a.y + (size_t)t * H + col;
             yp[0] = y4.x; yp[1] = y4.y; yp[2] = y4.z; yp[3] = y4.w;
+            if (a.x_next) {  // the next layer's input: bf16(x + y), each sum in fp32
+              const uint2 xv = __ldcg(reinterpret_cast<const uint2*>(a.xg + (size_t)t * H + col));
+              const float s0 = bf16_to_f((uint16_t)(xv.x & 0xffffu)) + y4.x;
+              const float s1 = bf16_to_f((uint16_t)(xv.x >> 16)) + y4.y;
+              const float s2 = bf16_to_f((uint16_t)(xv.y & 0xffffu)) + y4.z;
+              const float s3 = bf16_to_f((uint16_t)(xv.y >> 16)) + y4.w;
+              uint2 o;
+              o.x = (uint32_t)bf16_bits(s0) | ((uint32_t)bf16_bits(s1) << 16);
+              o.y = (uint32_t)bf16_bits(s2) | ((uint32_t)bf16_bits(s3) << 16);
+              *reinterpret_cast<uint2*>(a.x_next + (size_t)t * H + col) = o;
+            }
           }
         }
       }
@@ -1082,6 +1099,51 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(const __grid_
 // CTA per SM, all resident (a cooperative launch); every wait is bounded: a
 // CTA that gave up, or a barrier that timed out, ends the launch after the
 // layer (the status word says which).
+// The router of a chained stack: logits[t][e] = sum_h x[t][h] * W_r[e][h],
+// bf16 operands (products exact in fp32), fp32 sums in a fixed order: lane j
+// of a warp takes h = 8 j .. 8 j + 7 (mod 256) in increasing h (one fma
+// chain), then the 32 lane sums meet in the tree (a, a ^ 16), ..., (a, a ^ 1). CTA b computes the
+// experts b, b + G, ...; its warps take the (expert, row) pairs in turn.
+__device__ __forceinline__ void router_gemv(const Args& a, int G, int bid) {
+  const int T = a.T, E = a.E, H = a.H;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (bid >= E) return;
+  const int ne = (E - bid + G - 1) / G;
+  for (int pi = warp; pi < ne * T; pi += kWarps) {
+    const int e = bid + (pi / T) * G, t = pi - (pi / T) * T;
+    const uint16_t* wr = a.router_w + (size_t)e * H;
+    const uint16_t* xr = a.xg + (size_t)t * H;
+    float s = 0.f;
+    for (int hb = lane * 8; hb < H; hb += 8 * 256) {  // 8 steps' loads in flight together
+      uint4 wv[8], xv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        wv[u] = make_uint4(0u, 0u, 0u, 0u);
+        xv[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (hb + 256 * u < H) {
+          wv[u] = __ldg(reinterpret_cast<const uint4*>(wr + hb + 256 * u));
+          // written in this launch by the layer before: read from L2
+          xv[u] = __ldcg(reinterpret_cast<const uint4*>(xr + hb + 256 * u));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (hb + 256 * u >= H) continue;
+        const uint32_t wa[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+        const uint32_t xa[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          s = fmaf(bf16_to_f((uint16_t)(xa[i] & 0xffffu)), bf16_to_f((uint16_t)(wa[i] & 0xffffu)), s);
+          s = fmaf(bf16_to_f((uint16_t)(xa[i] >> 16)), bf16_to_f((uint16_t)(wa[i] >> 16)), s);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) const_cast<float*>(a.logits)[(size_t)t * E + e] = s;
+  }
+}
+
 constexpr int kStackBar = 96, kStackAbort = 97, kStackDone = 98;
 constexpr int kStackBase = 128, kStackStride = 32;  // layer l's counters: sync + base + stride l
 
@@ -1098,7 +1160,22 @@ decode_stack_kernel(const Args* __restrict__ plan, int L, int32_t* __restrict__ 
   __syncthreads();
   RingState& rs = s_rs;
   const int G = gridDim.x;
+  const bool routed = plan[0].router_w != nullptr;  // chained layers, router in the launch
+  int nbar = 0;  // grid barriers passed
   for (int l = 0; l < L; ++l) {
+    if (routed) {
+      // the router of layer l on its input (the caller's x for l = 0, else the
+      // x_next the layer before wrote), then a barrier that publishes the logits
+      if (l == 0) griddep_wait();
+      router_gemv(plan[l], G, blockIdx.x);
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        red_release_gpu_add(sync + kStackBar, 1);
+        s_stop = wait_counter_bounded(sync + kStackBar, (++nbar) * G, status) ? 0 : 1;
+      }
+      __syncthreads();
+      if (s_stop) break;
+    }
     const bool aborted = layer_body<MAXNT>(plan[l], rs, l == 0, false);
     if (threadIdx.x == 0) {
       // the next layer's descriptors, fetched while the barrier completes
@@ -1108,9 +1185,25 @@ decode_stack_kernel(const Args* __restrict__ plan, int L, int32_t* __restrict__ 
                                      &n.tm_gch, &n.tm_uch, &n.tm_dch, &n.tm_gsh, &n.tm_ush};
         for (const CUtensorMap* m : maps) prefetch_tensormap(m);
       }
-      if (aborted) atomicOr(sync + kStackAbort, 1);
-      red_release_gpu_add(sync + kStackBar, 1);
-      int stop = wait_counter_bounded(sync + kStackBar, (l + 1) * G, status) ? 0 : 1;
+      // unchained layers: a relaxed arrival, since nothing of layer l + 1
+      // reads what layer l wrote in this launch (its y goes out at the
+      // kernel's end; its partials were read into registers before the CTA
+      // got here); an abort flag is ordered before the arrival that announces it
+      if (aborted) {
+        atomicOr(sync + kStackAbort, 1);
+        __threadfence();
+      }
+      // chained layers: layer l's x_next is read by every CTA after this
+      // barrier (generic loads, and the TMA of the next layer's x boxes)
+      int stop;
+      if (routed) {
+        red_release_gpu_add(sync + kStackBar, 1);
+        stop = wait_counter_bounded(sync + kStackBar, (++nbar) * G, status) ? 0 : 1;
+        fence_proxy_async_global();
+      } else {
+        atomicAdd(sync + kStackBar, 1);
+        stop = wait_counter_relaxed(sync + kStackBar, (++nbar) * G, status) ? 0 : 1;
+      }
       if (ld_acquire_gpu(sync + kStackAbort)) stop = 1;
       s_stop = stop;
     }
@@ -1402,6 +1495,9 @@ static bool build_args(const FusedLaunch& f, fused::Args& a) {
   a.partial = f.partial;
   a.status = f.status; a.sync = f.sync;
   a.picks = f.picks;
+  a.router_w = f.router_w;
+  a.xg = static_cast<const uint16_t*>(f.x);
+  a.x_next = f.x_next;
   return true;
 }
 

@@ -110,6 +110,10 @@ struct FusedLaunch {
   int32_t* status;
   int32_t* sync;
   int32_t* picks;  // nullable: +1 per distinct routed expert (adaptive-cache counters)
+  // a chained stack with the router in the launch (else null): router weights
+  // [E][H] bf16 (logits written to `logits`), and the next layer's input
+  const uint16_t* router_w;
+  uint16_t* x_next;
 };
 bool fused_decode_supported(int H, int I, int shI, int T, bool x_bf16);
 // Slices of I per partial row of the one-launch path (the partial buffer holds

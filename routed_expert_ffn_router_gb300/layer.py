@@ -90,18 +90,30 @@ class MoeLayer:
 class DecodeStack:
     """Several layers' decode windows in one launch (moe_decode_stack): one
     workspace shared by the layers, a device plan of their kernel arguments
-    and each layer's output buffers. Marshalling only."""
+    and each layer's output buffers. Marshalling only.
 
-    def __init__(self, layers, logits, xs, T: int, slot_maps=None, device="cuda"):
-        """layers: sequence of synth.LayerInputs (device pools); logits[l] [T][E]
-        fp32 and xs[l] [T][H] bf16 device tensors, kept referenced here."""
+    Unchained (router_w None): each layer routes the given logits[l] and runs
+    on the given xs[l]. Chained (router_w: one [E][H] bf16 tensor per layer):
+    the launch computes each layer's logits from its input into self.logits[l]
+    and writes layer l + 1's input bf16(x_l + y_l) into self.xs[l + 1];
+    xs[0] is the caller's input."""
+
+    def __init__(self, layers, logits, xs, T: int, slot_maps=None, router_w=None, device="cuda"):
         self.device = torch.device(device)
         self.T = T
         self.L = len(layers)
         self.inps = list(layers)
         self.descs = [make_desc(inp) for inp in layers]
-        self.logits = list(logits)
-        self.xs = list(xs)
+        self.router_w = None if router_w is None else list(router_w)
+        if self.router_w is None:
+            self.logits = list(logits)
+            self.xs = list(xs)
+        else:
+            self.logits = [torch.empty(T, inp.cfg.E, dtype=torch.float32, device=self.device)
+                           for inp in layers]
+            H = layers[0].cfg.H
+            self.xs = [xs[0]] + [torch.empty(T, H, dtype=torch.int16, device=self.device)
+                                 for _ in range(self.L - 1)]
         # each layer's slot map (its LayerInputs' own unless given; None = all held)
         self.slot_maps = ([inp.slot_map for inp in layers] if slot_maps is None
                           else list(slot_maps))
@@ -133,8 +145,12 @@ class DecodeStack:
             raise ValueError("unsupported number of layers")
         self.plan = torch.empty(self.plan_bytes + 64, dtype=torch.uint8, device=self.device)
         self.plan_ptr = self.plan.data_ptr() + (-self.plan.data_ptr()) % 64
-        _lib.moe_decode_stack_prepare(self.descs, ios, T, self.plan_ptr, self.plan_bytes,
-                                      self.ws_ptr, self.ws_bytes)
+        if self.router_w is None:
+            _lib.moe_decode_stack_prepare(self.descs, ios, T, self.plan_ptr, self.plan_bytes,
+                                          self.ws_ptr, self.ws_bytes)
+        else:
+            _lib.moe_decode_stack_prepare_routed(self.descs, ios, self.router_w, T, self.plan_ptr,
+                                                 self.plan_bytes, self.ws_ptr, self.ws_bytes)
 
     def forward(self, stream=None):
         _lib.moe_decode_stack(self.plan_ptr, self.L, self.T, self.ws_ptr, self.ws_bytes, stream)

@@ -240,6 +240,14 @@ def clone_pool(inp: LayerInputs) -> LayerInputs:
                                down_q=inp.down_q.clone(), down_s=inp.down_s.clone(), sh=sh)
 
 
+def router_weights(cfg: MoeConfig, seed: int = 0, layer: int = 0, device="cpu") -> torch.Tensor:
+    """A layer's router weights for a chained stack: [E][H] bf16 bit patterns
+    (uint16), N(0, cfg.wg_std) rounded to bf16, from their own seed stream."""
+    g = _gen(seed * 1_000_003 + layer + 500_009, device)
+    w = torch.randn(cfg.E, cfg.H, generator=g, device=device) * cfg.wg_std
+    return f32_to_bf16_bits(w).contiguous()
+
+
 def random_slot_map(E: int, frac: float, seed: int) -> torch.Tensor:
     """Seeded random residency (used to exercise the miss path): slots in id order."""
     g = _gen(seed, "cpu")

@@ -116,3 +116,65 @@ def test_two_calls_in_a_row_and_a_longer_stack():
         assert torch.equal(a["y"], b["y"]) and torch.equal(a["w"], b["w"])
     _assert_same_as_single(layers[:3], first[:3], 4)
     _assert_same_as_single(layers[-2:], first[-2:], 4)
+
+
+def _assert_weights_match(w_gpu, w_orc, w_exact):
+    """Bitwise, except that a weight whose exact value sits at an fp32 rounding
+    midpoint (within 2^-40 relative) may round to either neighbour."""
+    w_gpu = np.asarray(w_gpu, np.float32)
+    for idx in np.argwhere(w_gpu != w_orc):
+        idx = tuple(idx)
+        a, b = w_gpu[idx], w_orc[idx]
+        assert abs(int(a.view(np.int32)) - int(b.view(np.int32))) == 1, (idx, a, b)
+        mid = (float(a) + float(b)) / 2
+        assert abs(w_exact[idx] - mid) <= 2.0 ** -40 * abs(mid), (idx, a, b, w_exact[idx])
+
+
+def _bf16_rne(f32):
+    """fp32 -> bf16 bit patterns, round to nearest even (finite values)."""
+    u = np.ascontiguousarray(f32, np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_routed_chained_stack_layer_by_layer(T):
+    """The router in the launch and layers chained through the residual: each
+    layer checked on the GPU's own input for that layer. Its logits against the
+    oracle's router (float64, rounded once) to fp32 rounding of the sum; its
+    routing bit for bit against the oracle's routing of the GPU logits; its y
+    within the gate; the next layer's input bit for bit against
+    bf16(x + y); and the whole layer bitwise equal to moe_layer_forward on
+    the same logits and input."""
+    cfg = synth.MoeConfig("stack_rt", H=2048, I=512, E=128, k=10, T=T)
+    L = 5
+    layers = _layers(cfg, L, T, seed=3)
+    wr = [synth.router_weights(cfg, 3, layer=l, device=DEV) for l in range(L)]
+    st = DecodeStack(layers, None, [layers[0].x] + [None] * (L - 1), T, router_w=wr)
+    st.forward()
+    torch.cuda.synchronize()
+    code, bits = st.status()
+    assert code == _lib.MOE_OK, f"device status {bits}"
+    outs = st.outs
+    for l in range(L):
+        x_bits = st.xs[l].cpu().numpy().view(np.uint16)
+        x_f32 = synth.bf16_bits_to_f32(x_bits)
+        w_f32 = synth.bf16_bits_to_f32(wr[l].cpu().numpy().view(np.uint16))
+        lg = st.logits[l].cpu().numpy()
+        lo = oracle.router_logits(x_f32, np.ascontiguousarray(w_f32.T))
+        assert np.abs(lg - lo).max() <= 1e-5 * np.abs(lo).max() + 1e-6, f"layer {l}: router logits"
+        ids, w, we = oracle.route(lg, cfg.k)
+        assert np.array_equal(outs[l]["ids"].cpu().numpy(), ids), f"layer {l}: ids"
+        _assert_weights_match(outs[l]["w"].cpu().numpy(), w, we)
+        inp = layers[l].to("cpu")
+        y_ref = oracle.Layer(inp).rows(ids, w, x=x_bits)
+        y = outs[l]["y"].cpu().double().numpy()
+        err = np.abs(y - y_ref).max()
+        assert err <= TOL * np.abs(y_ref).max(), f"layer {l}: {err:.3e}"
+        if l + 1 < L:
+            nxt = _bf16_rne(x_f32 + outs[l]["y"].cpu().numpy())
+            assert np.array_equal(st.xs[l + 1].cpu().numpy().view(np.uint16), nxt), f"layer {l}: residual"
+        # the same layer through one launch: bitwise
+        lay = MoeLayer(layers[l], T_max=T)
+        ref = lay.forward(st.logits[l], st.xs[l])
+        torch.cuda.synchronize()
+        assert torch.equal(ref["y"], outs[l]["y"]) and torch.equal(ref["w"], outs[l]["w"]), f"layer {l}"
