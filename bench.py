@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="bound on the oracle's CPU time for cpu_baseline")
     ap.add_argument("--profile-case", choices=["decode_window", "prefill", "expert_cache",
-                                               "decode48_T1"], default=None,
+                                               "decode48_T1", "decode48_stack_T1"], default=None,
                     help="run a few eager launches of one small case and exit (the target "
                          "of ncu captures: about 1 GB on the device, inputs larger than L2)")
     return ap.parse_args()
@@ -724,7 +724,7 @@ def extra_configs(torch, synth, _lib, dev, stream, hbm_peak, tf_peak, cpu_second
     (the whole layer per replay), with weight-pool copies rotated so that a
     replay's weights are not in L2 from the one before; beside each, the CPU
     oracle (one core) on a few rows of the same layer, scaled to the layer."""
-    from routed_expert_ffn_router_gb300.layer import MoeLayer
+    from routed_expert_ffn_router_gb300.layer import DecodeStack, MoeLayer
     out = {"cpu_oracle_host": host_facts()}
 
     def timed(fn, reps):
@@ -784,6 +784,34 @@ def extra_configs(torch, synth, _lib, dev, stream, hbm_peak, tf_peak, cpu_second
                         "frac_hbm": round(byts / ms / 1e6 / hbm_peak, 3),
                         "rows_per_s": round(T / (ms * 1e-3 / cfg.layers), 1),
                         "mean_distinct_experts": round(D / cfg.layers, 2)}
+        # the same 48 windows as one launch (moe_decode_stack): bitwise the same y
+        stk = DecodeStack(layers, [l.logits[:T] for l in layers], [l.x[:T] for l in layers], T)
+        stk.forward(stream=stream)
+        torch.cuda.synchronize()
+        assert all(torch.equal(a["y"], b["y"]) for a, b in zip(stk.outs, outs)), "stack != layers"
+        ms_s = timed(lambda i: stk.forward(stream=stream), 4)
+        res[f"T{T}"]["stack_us_per_layer"] = round(ms_s * 1e3 / cfg.layers, 2)
+        res[f"T{T}"]["stack_frac_hbm"] = round(byts / ms_s / 1e6 / hbm_peak, 3)
+        del stk
+    # the chained pass with the router in the launch (moe_decode_stack_prepare_routed):
+    # layer l + 1's input is bf16(x_l + y_l), its logits x W_r^T (W_r [E][H] bf16)
+    wr = [synth.router_weights(cfg, 0, layer=l, device=dev) for l in range(cfg.layers)]
+    for T in (1, 16):
+        stk = DecodeStack(layers, None, [layers[0].x[:T]] + [None] * (cfg.layers - 1), T,
+                          router_w=wr)
+        stk.forward(stream=stream)
+        torch.cuda.synchronize()
+        D = sum(int(torch.unique(o["ids"]).numel()) for o in stk.outs)
+        ms_r = timed(lambda i: stk.forward(stream=stream), 4)
+        byts = D * cfg.expert_bytes() + cfg.layers * cfg.E * cfg.H * 2
+        res[f"routed_T{T}"] = {"us_per_layer": round(ms_r * 1e3 / cfg.layers, 2),
+                               "GB/s": round(byts / ms_r / 1e6, 1),
+                               "frac_hbm": round(byts / ms_r / 1e6 / hbm_peak, 3),
+                               "mean_distinct_experts": round(D / cfg.layers, 2),
+                               "note": "router weights unbiased: routing near uniform, so more "
+                                       "experts per window than the Zipf-biased logits"}
+        del stk
+    del wr
     res["l2"] = "48 layers in turn (43.5 GB)"
     res["cpu_oracle_T16"] = cpu_leg(layers[0], list(range(16)), 16)
     out["decode48"] = res
@@ -837,6 +865,17 @@ def run_profile_case(case: str):
 
         def fn(i):
             lay.forward(logits[i % 4], xs[i % 4], out=out)
+        n = 6
+    elif case == "decode48_stack_T1":
+        # 4 layers of the 48-layer shape (3.6 GB) in one stack launch, 1-row windows
+        from routed_expert_ffn_router_gb300.layer import DecodeStack
+        cfg = synth.DECODE_48.with_T(1)
+        layers = [synth.make_layer(cfg, 0, device=dev, layer=l, T=1) for l in range(4)]
+        stk = DecodeStack(layers, [l.logits for l in layers], [l.x for l in layers], 1)
+        lay = stk
+
+        def fn(i):
+            stk.forward()
         n = 6
     else:
         cfg = synth.PREFILL
