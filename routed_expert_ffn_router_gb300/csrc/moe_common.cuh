@@ -21,6 +21,7 @@ enum : int32_t {
   DEV_BAD_SLOT = 2,          // slot_map[e] >= S (treated as not resident)
   DEV_TIMEOUT = 4,           // a bounded wait expired
   DEV_RANGE = 8,             // an activation outside the fp16 range (prefill path)
+  DEV_PLAN = 16,             // a stack launch whose layers or rows differ from its plan's
 };
 
 constexpr int kMaxK = 32;

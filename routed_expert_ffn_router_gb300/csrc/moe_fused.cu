@@ -121,6 +121,7 @@ struct Args {
   const uint16_t* router_w;
   const uint16_t* xg;  // x [T][H] bf16 for the router and the residual add
   uint16_t* x_next;
+  int stack_L;         // a stack plan's layer count (the launch checks it against its own)
 };
 
 // Stage layouts (byte offsets from the 1024-aligned stage base), UI = 32 MT
@@ -1149,9 +1150,18 @@ constexpr int kStackBase = 128, kStackStride = 32;  // layer l's counters: sync 
 
 template <int MAXNT>
 __global__ void __launch_bounds__(kThreads, 1)
-decode_stack_kernel(const Args* __restrict__ plan, int L, int32_t* __restrict__ sync,
-                    int32_t* __restrict__ status) {
+decode_stack_kernel(const Args* __restrict__ plan, int L, int T, int nst,
+                    int32_t* __restrict__ sync, int32_t* __restrict__ status) {
   __shared__ int s_stop;
+  // the launch's layer count, row tile and ring depth must be the plan's (its
+  // shared-memory layout is the plan's): else nothing runs and the status says so
+  {
+    const Args& p0 = plan[0];
+    if (p0.stack_L != L || p0.T != T || p0.TB != (MAXNT == 1 ? 8 : 16) || p0.nst != nst) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, DEV_PLAN);
+      return;
+    }
+  }
   // the ring state lives in shared memory between layers (each role reads it
   // at a layer's start and its owner writes it back at the end), so that no
   // register is held across the layers
@@ -1527,6 +1537,7 @@ cudaError_t fused_stack_prepare(const FusedLaunch* layers, int L, void* plan, cu
     if (f.T != layers[0].T || !build_args(f, a)) return cudaErrorInvalidValue;
     a.stage_bytes = fused::stage_bytes_for(fused::kMT, a.TB);
     a.nst = nst;
+    a.stack_L = L;
   }
   cudaError_t e = cudaMemcpyAsync(plan, h.data(), h.size() * sizeof(fused::Args),
                                   cudaMemcpyHostToDevice, st);
@@ -1535,8 +1546,8 @@ cudaError_t fused_stack_prepare(const FusedLaunch* layers, int L, void* plan, cu
 }
 
 template <int NTX>
-static cudaError_t launch_stack_nt(const fused::Args* plan, int L, int TB, int nst, int32_t* sync,
-                                   int32_t* status, cudaStream_t st) {
+static cudaError_t launch_stack_nt(const fused::Args* plan, int L, int T, int TB, int nst,
+                                   int32_t* sync, int32_t* status, cudaStream_t st) {
   constexpr int MT = fused::kMT;
   const size_t smem = fused::smem_bytes(MT, NTX, nst, fused::stage_bytes_for(MT, TB), TB);
   static std::mutex mu;
@@ -1572,7 +1583,8 @@ static cudaError_t launch_stack_nt(const fused::Args* plan, int L, int TB, int n
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   launch_begin(K_FUSED_STACK, st);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, fused::decode_stack_kernel<NTX>, plan, L, sync, status);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, fused::decode_stack_kernel<NTX>, plan, L, T, nst, sync,
+                                     status);
   launch_end(st);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -1585,8 +1597,8 @@ cudaError_t launch_fused_stack(const void* plan, int L, int T, int32_t* sync, in
   const int nst = TB == 8 ? stages_for<1, true>(TB) : stages_for<2, true>(TB);
   if (nst < 2) return cudaErrorInvalidValue;
   const fused::Args* p = static_cast<const fused::Args*>(plan);
-  return TB == 8 ? launch_stack_nt<1>(p, L, TB, nst, sync, status, st)
-                 : launch_stack_nt<2>(p, L, TB, nst, sync, status, st);
+  return TB == 8 ? launch_stack_nt<1>(p, L, T, TB, nst, sync, status, st)
+                 : launch_stack_nt<2>(p, L, T, TB, nst, sync, status, st);
 }
 
 }  // namespace moe

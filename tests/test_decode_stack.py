@@ -178,3 +178,27 @@ def test_routed_chained_stack_layer_by_layer(T):
         ref = lay.forward(st.logits[l], st.xs[l])
         torch.cuda.synchronize()
         assert torch.equal(ref["y"], outs[l]["y"]) and torch.equal(ref["w"], outs[l]["w"]), f"layer {l}"
+
+
+def test_a_launch_that_differs_from_its_plan_runs_nothing():
+    """moe_decode_stack with another layer count or row count than the plan's
+    (here: more or fewer layers, 12 rows on a 4-row plan, 5 rows on it) ORs
+    16 into the status word and leaves every output untouched; the prepared
+    launch then runs as usual."""
+    cfg = synth.MoeConfig("stack_guard", H=1024, I=512, E=32, k=4, T=4, zipf_s=1.0)
+    layers = _layers(cfg, 2, 4, seed=5)
+    st = DecodeStack(layers, [l.logits for l in layers], [l.x for l in layers], 4)
+    for o in st.outs:
+        o["y"].fill_(7.0)
+    for L, T in ((3, 4), (1, 4), (2, 12), (2, 5)):
+        _lib.moe_workspace_init(st.ws_ptr, st.ws_bytes)
+        _lib.moe_decode_stack(st.plan_ptr, L, T, st.ws_ptr, st.ws_bytes)
+        torch.cuda.synchronize()
+        code, bits = st.status()
+        assert code == _lib.MOE_ERR_DEVICE and bits & 16, (L, T, code, bits)
+        assert all(bool((o["y"] == 7.0).all()) for o in st.outs), (L, T)
+    _lib.moe_workspace_init(st.ws_ptr, st.ws_bytes)
+    outs = st.forward()
+    torch.cuda.synchronize()
+    assert st.status()[0] == _lib.MOE_OK
+    _assert_same_as_single(layers, [{k: v.clone() for k, v in o.items()} for o in outs], 4)
