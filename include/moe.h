@@ -44,8 +44,8 @@
  *    clamped); 4 a bounded wait expired after about a second (the call's
  *    results are incomplete); 8 an intermediate value beyond the fp16 range
  *    (an expert's SwiGLU output |h| >= 65504; the affected rows are
- *    unspecified); 16 a moe_decode_stack launch whose n_layers or T differ
- *    from its plan's (nothing ran).
+ *    unspecified); 16 a moe_decode_stack launch whose n_layers, T or
+ *    workspace differ from its plan's (nothing ran).
  *  - Results are deterministic: run to run, and for the decode path (T <= 16)
  *    a row's output does not depend on the other rows of the window.
  *  - A workspace serves one call at a time: calls that share one must be
@@ -238,9 +238,9 @@ moe_status moe_decode_stack_prepare_routed(const moe_layer_desc *layers, const m
                                            size_t ws_bytes, void *stream);
 
 /* Run the prepared stack: one cooperative launch on `stream` (one CTA per SM,
- * all resident; MOE_ERR_CUDA if the device cannot hold them all). n_layers
- * and T as prepared (the kernel checks them against the plan: a mismatch ORs
- * 16 into the status word and runs nothing); ws the prepared workspace. Asynchronous and capturable
+ * all resident; MOE_ERR_CUDA if the device cannot hold them all). n_layers,
+ * T and ws as prepared (the kernel checks them against the plan: a mismatch
+ * ORs 16 into the status word of the ws given and runs nothing). Asynchronous and capturable
  * once the plan exists. Device-detected problems go to ws's status word as for
  * moe_layer_forward; a CTA that gives up (an expired bounded wait) ends the
  * launch after its layer, and the later layers' outputs are left unwritten. */

@@ -1153,11 +1153,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 decode_stack_kernel(const Args* __restrict__ plan, int L, int T, int nst,
                     int32_t* __restrict__ sync, int32_t* __restrict__ status) {
   __shared__ int s_stop;
-  // the launch's layer count, row tile and ring depth must be the plan's (its
-  // shared-memory layout is the plan's): else nothing runs and the status says so
+  // the launch's layer count, rows, row tile, ring depth and workspace must be
+  // the plan's (its shared-memory layout and counters are the plan's): else
+  // nothing runs and the status word of the launch's workspace says so
   {
     const Args& p0 = plan[0];
-    if (p0.stack_L != L || p0.T != T || p0.TB != (MAXNT == 1 ? 8 : 16) || p0.nst != nst) {
+    if (p0.stack_L != L || p0.T != T || p0.TB != (MAXNT == 1 ? 8 : 16) || p0.nst != nst ||
+        p0.status != status) {
       if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, DEV_PLAN);
       return;
     }

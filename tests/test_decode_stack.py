@@ -181,10 +181,10 @@ def test_routed_chained_stack_layer_by_layer(T):
 
 
 def test_a_launch_that_differs_from_its_plan_runs_nothing():
-    """moe_decode_stack with another layer count or row count than the plan's
-    (here: more or fewer layers, 12 rows on a 4-row plan, 5 rows on it) ORs
-    16 into the status word and leaves every output untouched; the prepared
-    launch then runs as usual."""
+    """moe_decode_stack with another layer count, row count or workspace than
+    the plan's (here: more or fewer layers, 12 rows on a 4-row plan, 5 rows on
+    it, a second workspace) ORs 16 into the status word of the workspace given
+    and leaves every output untouched; the prepared launch then runs as usual."""
     cfg = synth.MoeConfig("stack_guard", H=1024, I=512, E=32, k=4, T=4, zipf_s=1.0)
     layers = _layers(cfg, 2, 4, seed=5)
     st = DecodeStack(layers, [l.logits for l in layers], [l.x for l in layers], 4)
@@ -197,6 +197,15 @@ def test_a_launch_that_differs_from_its_plan_runs_nothing():
         code, bits = st.status()
         assert code == _lib.MOE_ERR_DEVICE and bits & 16, (L, T, code, bits)
         assert all(bool((o["y"] == 7.0).all()) for o in st.outs), (L, T)
+    # another workspace than the plan's
+    other = torch.empty(st.ws_bytes + 256, dtype=torch.uint8, device=DEV)
+    optr = other.data_ptr() + (-other.data_ptr()) % 256
+    _lib.moe_workspace_init(optr, st.ws_bytes)
+    _lib.moe_decode_stack(st.plan_ptr, 2, 4, optr, st.ws_bytes)
+    torch.cuda.synchronize()
+    code, bits = _lib.moe_read_status(optr)
+    assert code == _lib.MOE_ERR_DEVICE and bits & 16, (code, bits)
+    assert all(bool((o["y"] == 7.0).all()) for o in st.outs)
     _lib.moe_workspace_init(st.ws_ptr, st.ws_bytes)
     outs = st.forward()
     torch.cuda.synchronize()
